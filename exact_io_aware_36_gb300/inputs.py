@@ -1,0 +1,218 @@
+"""Seeded synthetic workloads for exact attention.
+
+This module only draws random numbers, rounds them to the storage type and
+packs sequences.  It holds none of the attention arithmetic, so both the CUDA
+path and the fp64 oracle can take their inputs from here without sharing any
+of the method.
+
+Shapes follow the token-major layout of the FlashAttention user API
+("FlashAttention: Faster Attention Without Dropping a Single Interaction",
+Usage contract: ``flash_attn_func(q, k, v, dropout_p, softmax_scale, causal)``
+with scale, causal flag and Q/KV lengths):
+
+* ``q``, ``do``: ``[T, Hq, d]``; ``k``, ``v``: ``[T, Hkv, d]``; ``T`` the total
+  token count (``B * N`` dense, ``cu_seqlens[B]`` packed).
+* ``cu_seqlens``: int32 ``[B + 1]`` prefix sums of the sequence lengths, the
+  packed ("varlen") layout of "FlashAttention: The Algorithm That Beat the
+  Memory Wall", section "Varlen Is the Quiet Superpower".
+* ``alibi_slopes``: fp32 ``[Hq]``, slope of query head ``h`` (1-indexed)
+  ``2**(-8 h / Hq)``.
+
+Draw recipe (one fresh ``numpy.random.Generator(PCG64(seed))`` per workload):
+sequence lengths first (packed workloads only, ``integers(lo, hi + 1)``),
+then ``q, k, v, do`` as ``standard_normal(dtype=float32)`` in that order;
+``qk_gain`` multiplies q and k after the draw; bf16 workloads round every
+tensor to bf16 with round-to-nearest-even.  The fp32 arrays returned for bf16
+workloads hold exactly the bf16 values, so an fp64 upcast sees the same
+numbers the GPU sees.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field, replace
+from typing import Optional
+
+import numpy as np
+
+__all__ = [
+    "Workload", "WORKLOADS", "workload", "make_inputs", "small_case",
+    "bf16_round", "bf16_bits", "bf16_from_bits", "alibi_slopes",
+    "attended_pairs",
+]
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One synthetic attention problem.
+
+    ``N`` is the sequence length of dense workloads and the maximum length of
+    packed ones.  ``seqlen_range`` makes the workload packed: ``B`` lengths are
+    drawn uniformly from the closed range.
+    """
+    name: str
+    dtype: str                 # "bf16" or "fp32": storage / MMA operand type
+    causal: bool
+    B: int
+    Hq: int
+    Hkv: int
+    N: int
+    d: int
+    backward: bool = True
+    alibi: bool = False
+    qk_gain: float = 1.0
+    seqlen_range: Optional[tuple] = None
+    seqlens: Optional[tuple] = None   # explicit packed lengths (tests)
+    note: str = ""
+
+    @property
+    def varlen(self) -> bool:
+        return self.seqlen_range is not None or self.seqlens is not None
+
+    @property
+    def scale(self) -> float:
+        return float(1.0 / np.sqrt(self.d))
+
+
+# The five workloads the build is measured and checked on.
+WORKLOADS = {
+    "c1_fp32_fwd": Workload(
+        "c1_fp32_fwd", "fp32", causal=False, B=1, Hq=1, Hkv=1, N=128, d=64,
+        backward=False, note="fp32 forward only, non-causal, B=1 H=1 N=128 d=64"),
+    "c2_gpt2m": Workload(
+        "c2_gpt2m", "bf16", causal=True, B=8, Hq=16, Hkv=16, N=1024, d=64,
+        note="GPT-2-medium attention shape, causal, B=8 H=16 N=1024 d=64"),
+    "c3_long": Workload(
+        "c3_long", "bf16", causal=True, B=1, Hq=32, Hkv=32, N=16384, d=128,
+        qk_gain=0.5, note="long-context causal, B=1 H=32 N=16384 d=128, q,k x0.5"),
+    "c4_varlen": Workload(
+        "c4_varlen", "bf16", causal=True, B=64, Hq=32, Hkv=32, N=4096, d=128,
+        seqlen_range=(128, 4096),
+        note="64 packed sequences, lengths U[128,4096], causal, H=32 d=128"),
+    "c5_gqa_alibi": Workload(
+        "c5_gqa_alibi", "bf16", causal=True, B=2, Hq=32, Hkv=4, N=8192, d=128,
+        alibi=True, note="GQA 32/4 with ALiBi, causal, B=2 N=8192 d=128"),
+}
+
+
+def workload(name: str) -> Workload:
+    return WORKLOADS[name]
+
+
+def small_case(dtype="bf16", causal=True, B=1, Hq=2, Hkv=2, N=128, d=64,
+               alibi=False, seqlens=None, qk_gain=1.0, backward=True,
+               name="small") -> Workload:
+    """A small workload for parity tests (explicit packed lengths allowed)."""
+    if seqlens is not None:
+        seqlens = tuple(int(x) for x in seqlens)
+        B = len(seqlens)
+        N = max(seqlens) if seqlens else 0
+    return Workload(name, dtype, causal, B, Hq, Hkv, N, d, backward=backward,
+                    alibi=alibi, qk_gain=qk_gain, seqlens=seqlens)
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns of float32 ``x`` with round-to-nearest-even."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    rounding = ((u >> 16) & 1) + np.uint32(0x7FFF)
+    out = ((u + rounding) >> 16).astype(np.uint16)
+    nan = np.isnan(x)
+    if nan.any():
+        out[nan] = np.uint16(0x7FC0)
+    return out
+
+
+def bf16_from_bits(b: np.ndarray) -> np.ndarray:
+    """float32 values of bf16 bit patterns (exact)."""
+    return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    return bf16_from_bits(bf16_bits(x))
+
+
+def alibi_slopes(Hq: int) -> np.ndarray:
+    """ALiBi slope of each query head: 2**(-8 h / Hq) for h = 1..Hq."""
+    h = np.arange(1, Hq + 1, dtype=np.float64)
+    return np.exp2(-8.0 * h / Hq).astype(np.float32)
+
+
+def _seqlens(w: Workload, rng: np.random.Generator) -> np.ndarray:
+    if w.seqlens is not None:
+        return np.asarray(w.seqlens, dtype=np.int64)
+    if w.seqlen_range is not None:
+        lo, hi = w.seqlen_range
+        return rng.integers(lo, hi + 1, size=w.B).astype(np.int64)
+    return np.full(w.B, w.N, dtype=np.int64)
+
+
+def attended_pairs(w: Workload, seqlens=None) -> int:
+    """Number of (query, key) pairs the workload attends, over heads and sequences.
+
+    Causal: L(L+1)/2 per sequence and query head; otherwise L*L.
+    """
+    if seqlens is None:
+        seqlens = make_seqlens(w)
+    L = np.asarray(seqlens, dtype=np.int64)
+    per = L * (L + 1) // 2 if w.causal else L * L
+    return int(per.sum()) * w.Hq
+
+
+def make_seqlens(w: Workload, seed: int = 0) -> np.ndarray:
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return _seqlens(w, rng)
+
+
+@dataclass
+class Inputs:
+    workload: Workload
+    seed: int
+    seqlens: np.ndarray
+    cu_seqlens: np.ndarray          # int32 [B+1]
+    q: np.ndarray                   # float32 [T, Hq, d] (bf16-exact for bf16)
+    k: np.ndarray                   # float32 [T, Hkv, d]
+    v: np.ndarray
+    do: Optional[np.ndarray]        # float32 [T, Hq, d]
+    alibi_slopes: Optional[np.ndarray]
+    scale: float
+    bits: dict = field(default_factory=dict)   # bf16 bit patterns (uint16)
+
+    @property
+    def T(self) -> int:
+        return int(self.cu_seqlens[-1])
+
+
+def make_inputs(w: Workload, seed: int = 0, with_do: Optional[bool] = None) -> Inputs:
+    """Draw the inputs of workload ``w`` following the recipe in the module doc."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    L = _seqlens(w, rng)
+    cu = np.zeros(len(L) + 1, dtype=np.int64)
+    cu[1:] = np.cumsum(L)
+    T = int(cu[-1])
+    if with_do is None:
+        with_do = w.backward
+
+    def draw(H):
+        x = rng.standard_normal(size=(T, H, w.d), dtype=np.float32)
+        return x
+
+    q = draw(w.Hq)
+    k = draw(w.Hkv)
+    v = draw(w.Hkv)
+    do = draw(w.Hq) if with_do else None
+    if w.qk_gain != 1.0:
+        q *= np.float32(w.qk_gain)
+        k *= np.float32(w.qk_gain)
+    bits = {}
+    if w.dtype == "bf16":
+        for name, x in (("q", q), ("k", k), ("v", v), ("do", do)):
+            if x is None:
+                continue
+            b = bf16_bits(x)
+            bits[name] = b
+            x[...] = bf16_from_bits(b)
+    slopes = alibi_slopes(w.Hq) if w.alibi else None
+    return Inputs(w, seed, L, cu.astype(np.int32), q, k, v, do, slopes, w.scale, bits)
+
+
+def with_seqlens(w: Workload, seqlens) -> Workload:
+    return replace(w, seqlens=tuple(int(x) for x in seqlens), B=len(seqlens),
+                   N=int(max(seqlens)), seqlen_range=None)

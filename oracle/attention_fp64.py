@@ -1,0 +1,417 @@
+"""fp64 CPU oracle for exact scaled-dot-product attention, forward and backward.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline / reference arm of ``bench.py`` may import or run this module.  The
+product (the CUDA library and its Python binding) never calls it, and it
+shares no code with the product: it depends on NumPy alone.
+
+Pages followed (cited by title and section):
+
+* [FA1 note] "FlashAttention: Faster Attention Without Dropping a Single
+  Interaction" (awesome.papernotes.org note on arXiv 2205.14135).
+  - Key design 1: S = QK^T/sqrt(d), P = softmax(S), O = PV.
+  - Key design 2: the mergeable (m, l, O) update and its table (FA2 stores
+    L = m + log l).
+  - Key design 3: D_i = dO_i . O_i and dS = P o (dP - D); dV = P^T dO,
+    dQ = dS K, dK = dS^T Q.
+  - Usage contract table: scale, causal flag, Q/KV lengths; ALiBi and MQA
+    named among the mask/variant features.
+* [Memory-wall page] "FlashAttention: The Algorithm That Beat the Memory
+  Wall" (repo-explainer.com), "A Tile, a Register File, and a Trick Called
+  Online Softmax" (per-step normalised recurrence) and "Varlen Is the Quiet
+  Superpower" (packed sequences).
+
+The plain definition is the oracle: for each (sequence, query head) it
+materialises S and P in float64 and applies the formulas above directly.  The
+method reaches that same result up to rounding order, so no step of the tiled
+algorithm is emulated here, except in ``online_softmax_forward`` which exists
+only so the tests can check the pages' recurrence against the definition.
+
+Readings where the pages are silent or ambiguous (each also stated where used):
+
+R1  A bias or mask is added after the 1/sqrt(d) scaling and is not scaled.
+R2  The FA1 note's backward sketch forms raw scores with no scale; by the chain
+    rule dQ and dK carry the factor ``scale`` and dV does not.
+R3  "log" in L = m + log l is the natural logarithm.
+R4  ALiBi: bias[i, j] = -slope_h * (i - j), i the query and j the key position
+    local to the sequence; slopes are per query head.
+R5  GQA/MQA: contiguous groups, kv head g = h // (Hq / Hkv); dK and dV of a kv
+    head are sums over its query heads.
+R6  Causal: key j visible to query i iff j <= i, positions local to the
+    sequence; query and key lengths are equal per sequence.
+R7  A row with no visible key (cannot occur under R6) gets O = 0, LSE = -inf.
+R8  No dropout (the usage contract's example passes dropout_p = 0.0).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "attention_forward", "attention_backward", "head_forward", "head_backward",
+    "head_scores", "online_softmax_forward", "online_softmax_forward_normalised",
+    "forward_rows", "backward_query_rows", "backward_key_rows", "head_row_stats",
+]
+
+
+def _f64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+def head_scores(q, k, scale, causal, slope=None):
+    """Scores of one (sequence, head): S = scale * q k^T + bias, masked.
+
+    [FA1 note] Key design 1, S = QK^T / sqrt(d) with ``scale`` in place of
+    1/sqrt(d) (usage contract: softmax_scale).  ALiBi bias per R4, added after
+    scaling (R1).  Causal mask per R6: masked entries are -inf.
+    """
+    q = _f64(q)
+    k = _f64(k)
+    L = q.shape[0]
+    S = scale * (q @ k.T)
+    if slope is not None:
+        i = np.arange(L, dtype=np.float64)[:, None]
+        j = np.arange(k.shape[0], dtype=np.float64)[None, :]
+        S = S - float(slope) * (i - j)
+    if causal:
+        vis = np.arange(k.shape[0])[None, :] <= np.arange(L)[:, None]
+        S = np.where(vis, S, -np.inf)
+    return S
+
+
+def _softmax_rows(S):
+    """P = softmax(S) row-wise and LSE = m + log(l) (R3, R7)."""
+    m = S.max(axis=1, initial=-np.inf) if S.shape[1] else np.full(S.shape[0], -np.inf)
+    finite = np.isfinite(m)
+    m_safe = np.where(finite, m, 0.0)
+    E = np.exp(S - m_safe[:, None])
+    E[~finite] = 0.0
+    l = E.sum(axis=1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        P = np.where(l[:, None] > 0, E / np.where(l > 0, l, 1.0)[:, None], 0.0)
+        lse = np.where(l > 0, m_safe + np.log(np.where(l > 0, l, 1.0)), -np.inf)
+    return P, lse
+
+
+def head_forward(q, k, v, scale, causal, slope=None):
+    """O and LSE of one (sequence, head), materialising S and P.
+
+    [FA1 note] Key design 1: P = softmax(S), O = P V.  Key design 2's table:
+    L = m + log l is saved per row for the backward (R3).
+    Returns (O, LSE, P).
+    """
+    S = head_scores(q, k, scale, causal, slope)
+    P, lse = _softmax_rows(S)
+    O = P @ _f64(v)
+    return O, lse, P
+
+
+def head_backward(q, k, v, do, scale, causal, slope=None):
+    """dQ, dK, dV of one (sequence, head) from the materialised P.
+
+    [FA1 note] Key design 3: dV = P^T dO; dP = dO V^T; D_i = rowsum(P o dP)
+    (equal to dO_i . O_i); dS = P o (dP - D); dQ = dS K, dK = dS^T Q with the
+    chain-rule factor ``scale`` (R2).  The bias has no gradient.
+    Returns (dQ, dK, dV, O, LSE, D).
+    """
+    q = _f64(q)
+    k = _f64(k)
+    v = _f64(v)
+    do = _f64(do)
+    O, lse, P = head_forward(q, k, v, scale, causal, slope)
+    dV = P.T @ do
+    dP = do @ v.T
+    D = (P * dP).sum(axis=1)
+    dS = P * (dP - D[:, None])
+    dQ = scale * (dS @ k)
+    dK = scale * (dS.T @ q)
+    return dQ, dK, dV, O, lse, D
+
+
+def _layout(q, k, cu_seqlens):
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    if cu_seqlens is None:
+        cu = np.array([0, T], dtype=np.int64)
+    else:
+        cu = np.asarray(cu_seqlens, dtype=np.int64)
+    return T, Hq, Hkv, d, cu
+
+
+def _slope(alibi_slopes, h):
+    return None if alibi_slopes is None else float(alibi_slopes[h])
+
+
+def attention_forward(q, k, v, scale, causal, cu_seqlens=None, alibi_slopes=None,
+                      heads=None, seqs=None):
+    """O [T, Hq, d] and LSE [Hq, T] of packed multi-head attention.
+
+    Sequences are the segments [cu[b], cu[b+1]) of the token axis ([Memory-wall
+    page] Varlen); kv head of query head h per R5.  ``heads`` / ``seqs``
+    restrict the work to whole heads / sequences (other entries stay NaN).
+    """
+    T, Hq, Hkv, d, cu = _layout(q, k, cu_seqlens)
+    group = Hq // Hkv
+    O = np.full((T, Hq, v.shape[2]), np.nan)
+    LSE = np.full((Hq, T), np.nan)
+    for b in (range(len(cu) - 1) if seqs is None else seqs):
+        s, e = int(cu[b]), int(cu[b + 1])
+        for h in (range(Hq) if heads is None else heads):
+            g = h // group
+            o, lse, _ = head_forward(q[s:e, h], k[s:e, g], v[s:e, g], scale, causal,
+                                     _slope(alibi_slopes, h))
+            O[s:e, h] = o
+            LSE[h, s:e] = lse
+    return O, LSE
+
+
+def attention_backward(q, k, v, do, scale, causal, cu_seqlens=None, alibi_slopes=None,
+                       heads=None, seqs=None):
+    """dQ, dK, dV (plus O, LSE, D) of packed multi-head attention.
+
+    dK and dV of kv head g sum the contributions of its query heads (R5).
+    ``heads`` selects query heads; a kv head's dK/dV is complete only when all
+    of its group's query heads are selected.
+    """
+    T, Hq, Hkv, d, cu = _layout(q, k, cu_seqlens)
+    group = Hq // Hkv
+    dQ = np.full(q.shape, np.nan)
+    dK = np.zeros(k.shape)
+    dV = np.zeros(v.shape)
+    O = np.full((T, Hq, v.shape[2]), np.nan)
+    LSE = np.full((Hq, T), np.nan)
+    D = np.full((Hq, T), np.nan)
+    for b in (range(len(cu) - 1) if seqs is None else seqs):
+        s, e = int(cu[b]), int(cu[b + 1])
+        for h in (range(Hq) if heads is None else heads):
+            g = h // group
+            dq, dk, dv, o, lse, dd = head_backward(
+                q[s:e, h], k[s:e, g], v[s:e, g], do[s:e, h], scale, causal,
+                _slope(alibi_slopes, h))
+            dQ[s:e, h] = dq
+            dK[s:e, g] += dk
+            dV[s:e, g] += dv
+            O[s:e, h] = o
+            LSE[h, s:e] = lse
+            D[h, s:e] = dd
+    return dQ, dK, dV, O, LSE, D
+
+
+# --------------------------------------------------------------------------
+# The pages' recurrences, written out so that the tests can check them
+# against the definition above (exactness, FA1 Theorem 1).
+# --------------------------------------------------------------------------
+
+def online_softmax_forward(q, k, v, scale, causal, slope=None, block_q=1, block_k=1):
+    """Forward by the mergeable (m, l, O) state, FA1 loop order.
+
+    [FA1 note] Key design 1: K/V blocks in the outer loop, Q blocks in the
+    inner loop, state kept per query row.  Key design 2: for a new score tile
+    with row max m~ and local sum l~ of P~ = exp(S - m~):
+        m' = max(m, m~),  l' = e^(m - m') l + e^(m~ - m') l~,
+        O' = (e^(m - m') l O + e^(m~ - m') P~ V) / l'.
+    Returns (O, LSE) with LSE = m + log l (FA2, Key design 2's table).
+    """
+    q = _f64(q)
+    k = _f64(k)
+    v = _f64(v)
+    Lq, Lk = q.shape[0], k.shape[0]
+    O = np.zeros((Lq, v.shape[1]))
+    m = np.full(Lq, -np.inf)
+    l = np.zeros(Lq)
+    S_all = head_scores(q, k, scale, causal, slope)   # tiles are read from here
+    for ks in range(0, Lk, block_k):
+        ke = min(ks + block_k, Lk)
+        for qs in range(0, Lq, block_q):
+            qe = min(qs + block_q, Lq)
+            S = S_all[qs:qe, ks:ke]
+            m_t = S.max(axis=1)
+            ok = np.isfinite(m_t)
+            if not ok.any():
+                continue
+            P_t = np.zeros_like(S)
+            P_t[ok] = np.exp(S[ok] - m_t[ok, None])
+            l_t = P_t.sum(axis=1)
+            m_old, l_old, O_old = m[qs:qe], l[qs:qe], O[qs:qe]
+            m_new = np.maximum(m_old, np.where(ok, m_t, -np.inf))
+            a_old = np.where(np.isfinite(m_old), np.exp(m_old - m_new), 0.0)
+            a_new = np.where(ok, np.exp(np.where(ok, m_t, 0.0) - m_new), 0.0)
+            l_new = a_old * l_old + a_new * l_t
+            num = (a_old * l_old)[:, None] * O_old + a_new[:, None] * (P_t @ v[ks:ke])
+            O[qs:qe] = num / l_new[:, None]
+            m[qs:qe] = m_new
+            l[qs:qe] = l_new
+    lse = np.where(l > 0, m + np.log(np.where(l > 0, l, 1.0)), -np.inf)
+    return O, lse
+
+
+def online_softmax_forward_normalised(q, k, v, scale, causal, slope=None, block_k=1):
+    """Forward by the per-step normalised recurrence, one query tile.
+
+    [Memory-wall page] online-softmax sketch: per K/V tile, m_new = max(m,
+    max S); P = exp(S - m_new); l_new = e^(m - m_new) l + sum P;
+    O = (e^(m - m_new) l / l_new) O + (P V) / l_new.  The sketch calls l
+    "running_lse"; it is the running exponential sum (read as such).
+    """
+    q = _f64(q)
+    k = _f64(k)
+    v = _f64(v)
+    Lq, Lk = q.shape[0], k.shape[0]
+    S_all = head_scores(q, k, scale, causal, slope)
+    O = np.zeros((Lq, v.shape[1]))
+    m = np.full(Lq, -np.inf)
+    l = np.zeros(Lq)
+    for ks in range(0, Lk, block_k):
+        S = S_all[:, ks:ks + block_k]
+        m_new = np.maximum(m, S.max(axis=1))
+        live = np.isfinite(m_new)
+        P = np.zeros_like(S)
+        P[live] = np.exp(S[live] - m_new[live, None])
+        alpha = np.where(np.isfinite(m), np.exp(m - np.where(live, m_new, 0.0)), 0.0)
+        l_new = alpha * l + P.sum(axis=1)
+        safe = np.where(l_new > 0, l_new, 1.0)
+        O = np.where(live[:, None],
+                     (alpha * l / safe)[:, None] * O + (P @ v[ks:ks + block_k]) / safe[:, None],
+                     O)
+        m, l = np.where(live, m_new, m), np.where(live, l_new, l)
+    lse = np.where(l > 0, m + np.log(np.where(l > 0, l, 1.0)), -np.inf)
+    return O, lse
+
+
+# --------------------------------------------------------------------------
+# Row-sampled forms for workloads too large to materialise whole: each output
+# row is computed from its own definition, one at a time.
+# --------------------------------------------------------------------------
+
+def _seq_of(cu, t):
+    b = int(np.searchsorted(cu, t, side="right") - 1)
+    return b, int(cu[b]), int(cu[b + 1])
+
+
+def forward_rows(q, k, v, scale, causal, rows, cu_seqlens=None, alibi_slopes=None):
+    """O and LSE at sampled (token t, query head h) rows.
+
+    Row i of Key design 1's definition needs only q_i and the sequence's keys:
+    S_i = scale q_i k^T + bias_i (masked), P_i = softmax(S_i), O_i = P_i V.
+    Returns (O [n, d], LSE [n]).
+    """
+    T, Hq, Hkv, d, cu = _layout(q, k, cu_seqlens)
+    group = Hq // Hkv
+    outO, outL = [], []
+    for t, h in rows:
+        b, s, e = _seq_of(cu, t)
+        g = h // group
+        i = t - s
+        kk = _f64(k[s:e, g])
+        srow = scale * (kk @ _f64(q[t, h]))
+        if alibi_slopes is not None:
+            srow = srow - float(alibi_slopes[h]) * (i - np.arange(e - s, dtype=np.float64))
+        if causal:
+            srow = np.where(np.arange(e - s) <= i, srow, -np.inf)
+        P, lse = _softmax_rows(srow[None, :])
+        outO.append((P @ _f64(v[s:e, g]))[0])
+        outL.append(lse[0])
+    return np.array(outO), np.array(outL)
+
+
+def head_row_stats(q, k, v, do, scale, causal, s, e, h, g, slope=None, chunk=1024):
+    """LSE_i and D_i = dO_i . O_i of every query row of one (sequence, head).
+
+    Computed in row chunks (each chunk materialises its rows of S), so whole
+    long heads fit in memory.  D is None when ``do`` is None.
+    """
+    L = e - s
+    kk = _f64(k[s:e, g])
+    vv = _f64(v[s:e, g])
+    lse = np.empty(L)
+    D = None if do is None else np.empty(L)
+    for r0 in range(0, L, chunk):
+        r1 = min(r0 + chunk, L)
+        S = scale * (_f64(q[s + r0:s + r1, h]) @ kk.T)
+        i = np.arange(r0, r1, dtype=np.float64)[:, None]
+        j = np.arange(L, dtype=np.float64)[None, :]
+        if slope is not None:
+            S = S - slope * (i - j)
+        if causal:
+            S = np.where(j <= i, S, -np.inf)
+        P, lse[r0:r1] = _softmax_rows(S)
+        if D is not None:
+            D[r0:r1] = (_f64(do[s + r0:s + r1, h]) * (P @ vv)).sum(axis=1)
+    return lse, D
+
+
+def backward_query_rows(q, k, v, do, scale, causal, rows, cu_seqlens=None,
+                        alibi_slopes=None):
+    """dQ at sampled (token t, query head h) rows.
+
+    Row i of Key design 3: P_i from its scores, dP_i = dO_i V^T,
+    D_i = dO_i . O_i, dS_i = P_i o (dP_i - D_i), dQ_i = scale dS_i K (R2).
+    """
+    T, Hq, Hkv, d, cu = _layout(q, k, cu_seqlens)
+    group = Hq // Hkv
+    out = []
+    for t, h in rows:
+        b, s, e = _seq_of(cu, t)
+        g = h // group
+        i = t - s
+        kk = _f64(k[s:e, g])
+        vv = _f64(v[s:e, g])
+        srow = scale * (kk @ _f64(q[t, h]))
+        if alibi_slopes is not None:
+            srow = srow - float(alibi_slopes[h]) * (i - np.arange(e - s, dtype=np.float64))
+        if causal:
+            srow = np.where(np.arange(e - s) <= i, srow, -np.inf)
+        P, _ = _softmax_rows(srow[None, :])
+        P = P[0]
+        o = P @ vv
+        dOi = _f64(do[t, h])
+        dP = vv @ dOi
+        D = dOi @ o
+        dS = P * (dP - D)
+        out.append(scale * (dS @ kk))
+    return np.array(out)
+
+
+def backward_key_rows(q, k, v, do, scale, causal, rows, cu_seqlens=None,
+                      alibi_slopes=None, stats_cache=None):
+    """dK and dV at sampled (token t, kv head g) rows.
+
+    Column j of Key design 3's formulas: dV_j = sum_i P_ij dO_i and
+    dK_j = scale sum_i dS_ij q_i, summed over the query heads of g's group
+    (R5), with P_ij = exp(S_ij - LSE_i) and dS_ij = P_ij (dP_ij - D_i).  LSE_i
+    and D_i of every row come from ``head_row_stats``.
+    Returns (dK [n, d], dV [n, d]).
+    """
+    T, Hq, Hkv, d, cu = _layout(q, k, cu_seqlens)
+    group = Hq // Hkv
+    if stats_cache is None:
+        stats_cache = {}
+    outK, outV = [], []
+    for t, g in rows:
+        b, s, e = _seq_of(cu, t)
+        j = t - s
+        dk = np.zeros(d)
+        dv = np.zeros(v.shape[2])
+        for h in range(g * group, (g + 1) * group):
+            slope = _slope(alibi_slopes, h)
+            if (b, h) not in stats_cache:
+                stats_cache[(b, h)] = head_row_stats(q, k, v, do, scale, causal,
+                                                     s, e, h, g, slope)
+            lse, D = stats_cache[(b, h)]
+            qq = _f64(q[s:e, h])
+            dd = _f64(do[s:e, h])
+            i = np.arange(e - s, dtype=np.float64)
+            scol = scale * (qq @ _f64(k[t, g]))
+            if slope is not None:
+                scol = scol - slope * (i - j)
+            if causal:
+                scol = np.where(i >= j, scol, -np.inf)
+            Pcol = np.where(np.isfinite(scol), np.exp(scol - lse), 0.0)
+            dPcol = dd @ _f64(v[t, g])
+            dScol = Pcol * (dPcol - D)
+            dv += Pcol @ dd
+            dk += scale * (dScol @ qq)
+        outK.append(dk)
+        outV.append(dv)
+    return np.array(outK), np.array(outV)
