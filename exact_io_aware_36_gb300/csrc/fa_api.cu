@@ -1,0 +1,206 @@
+// fa_api.cu -- the C ABI of libfa (declared in include/fa.h): argument
+// checks, workspace sizing, the per-device status word and dispatch to the
+// kernels.  Every check runs before any launch; nothing here allocates
+// device memory.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "fa_internal.h"
+
+namespace {
+
+__device__ unsigned int g_fa_status;   // per-device status word
+
+constexpr int kMaxDevices = 64;
+
+unsigned int* status_ptr() {
+  static unsigned int* ptrs[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fa_status) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<unsigned int*>(p);
+  }
+  return ptrs[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Shared size checks of fa_fwd / fa_bwd.  Fills T.
+fa_status check_sizes(int B, int Hq, int Hkv, int N, int d, float scale,
+                      const int32_t* cu_seqlens, long long total_tokens, fa_dtype dtype,
+                      bool backward, long long* T) {
+  if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || total_tokens < 0) return FA_ERR_SHAPE;
+  if (Hq % Hkv != 0) return FA_ERR_SHAPE;
+  if (dtype != FA_BF16 && dtype != FA_FP32) return FA_ERR_UNSUPPORTED;
+  if (backward && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+  if (dtype == FA_BF16 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (dtype == FA_FP32 && d > 128) return FA_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_UNSUPPORTED;
+  if (B > 65535 || Hq > 65535) return FA_ERR_UNSUPPORTED;
+  const long long dense = (long long)B * N;
+  if (cu_seqlens == nullptr) {
+    if (total_tokens != 0 && total_tokens != dense) return FA_ERR_SHAPE;
+    *T = dense;
+  } else {
+    *T = total_tokens;
+  }
+  // token coordinates are 32-bit in the TMA descriptors and the kernels
+  if (*T >= (1ll << 31) || (long long)N >= (1ll << 30)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+fa::AttnParams base_params(int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                           const int32_t* cu_seqlens, long long T, const float* alibi) {
+  fa::AttnParams p = {};
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.d = d;
+  p.T = T;
+  p.group = Hq / Hkv;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = scale * fa::kLog2e;
+  p.cu_seqlens = cu_seqlens;
+  p.alibi = alibi;
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_version(void) { return 10000; }
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_NULL: return "a required pointer is NULL";
+    case FA_ERR_SHAPE: return "invalid or inconsistent sizes";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration (head dim, dtype or scale)";
+    case FA_ERR_ALIGN: return "a bf16 tensor is not 16-byte aligned";
+    case FA_ERR_WORKSPACE: return "workspace missing or too small";
+    case FA_ERR_CUDA: return "CUDA runtime or launch error";
+    case FA_ERR_DEVICE_TIMEOUT: return "device pipeline wait exceeded its time limit";
+    case FA_ERR_CU_SEQLENS: return "cu_seqlens malformed or a sequence longer than N";
+  }
+  return "unknown status";
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                 int Hkv, int N, int d, float scale, int causal, const int32_t* cu_seqlens,
+                 long long total_tokens, const float* alibi_slopes, fa_dtype dtype,
+                 fa_dtype o_dtype, void* stream) {
+  long long T = 0;
+  fa_status st = check_sizes(B, Hq, Hkv, N, d, scale, cu_seqlens, total_tokens, dtype, false, &T);
+  if (st != FA_OK) return st;
+  if (o_dtype != FA_FP32 && !(o_dtype == FA_BF16 && dtype == FA_BF16)) return FA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
+  if (dtype == FA_BF16 && (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)))
+    return FA_ERR_ALIGN;
+  if (dtype == FA_FP32 && ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                            reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o)) & 3u))
+    return FA_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_ALIGN;
+  if (T == 0 || B == 0 || N == 0) return FA_OK;
+  fa::AttnParams p = base_params(B, Hq, Hkv, N, d, scale, causal, cu_seqlens, T, alibi_slopes);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.lse = lse;
+  p.o_f32 = o_dtype == FA_FP32;
+  p.status = status_ptr();
+  if (!p.status) return FA_ERR_CUDA;
+  const int e = dtype == FA_FP32 ? fa::launch_fwd_fp32(p, stream) : fa::launch_fwd_bf16(p, stream);
+  return e == 0 ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, long long total_tokens) {
+  if (B < 0 || Hq <= 0 || N < 0 || d <= 0 || total_tokens < 0) return 0;
+  const long long T = total_tokens > 0 ? total_tokens : (long long)B * N;
+  return round256((size_t)Hq * T * sizeof(float)) + round256((size_t)Hq * T * d * sizeof(float));
+}
+
+static fa_status bwd_impl(int stage, const void* q, const void* k, const void* v, const void* o,
+                          const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                          int Hq, int Hkv, int N, int d, float scale, int causal,
+                          const int32_t* cu_seqlens, long long total_tokens,
+                          const float* alibi_slopes, fa_dtype dtype, fa_dtype o_dtype,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  long long T = 0;
+  fa_status st = check_sizes(B, Hq, Hkv, N, d, scale, cu_seqlens, total_tokens, dtype, true, &T);
+  if (st != FA_OK) return st;
+  if (o_dtype != FA_FP32 && o_dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+  if (stage < -1 || stage > 2) return FA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(lse))
+    return FA_ERR_ALIGN;
+  if (T == 0 || B == 0 || N == 0) return FA_OK;
+  const size_t need = fa_bwd_workspace_size(B, Hq, N, d, T);
+  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_ALIGN;
+  fa::AttnParams p = base_params(B, Hq, Hkv, N, d, scale, causal, cu_seqlens, T, alibi_slopes);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = const_cast<void*>(o);
+  p.lse = const_cast<float*>(lse);
+  p.o_f32 = o_dtype == FA_FP32;
+  p.dO = dO;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.D = static_cast<float*>(workspace);
+  p.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                      round256((size_t)Hq * T * sizeof(float)));
+  p.status = status_ptr();
+  if (!p.status) return FA_ERR_CUDA;
+  const int e = fa::launch_bwd_bf16(p, stream, stage);
+  return e == 0 ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                 const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
+                 int d, float scale, int causal, const int32_t* cu_seqlens,
+                 long long total_tokens, const float* alibi_slopes, fa_dtype dtype,
+                 fa_dtype o_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(-1, q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal,
+                  cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype, workspace,
+                  workspace_bytes, stream);
+}
+
+fa_status fa_bwd_stage(int stage, const void* q, const void* k, const void* v, const void* o,
+                       const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                       int Hq, int Hkv, int N, int d, float scale, int causal,
+                       const int32_t* cu_seqlens, long long total_tokens,
+                       const float* alibi_slopes, fa_dtype dtype, fa_dtype o_dtype,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  if (stage < 0 || stage > 2) return FA_ERR_UNSUPPORTED;
+  return bwd_impl(stage, q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal,
+                  cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype, workspace,
+                  workspace_bytes, stream);
+}
+
+fa_status fa_check_device_error(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned int* p = status_ptr();
+  if (!p) return FA_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (v != 0 && cudaMemset(p, 0, sizeof(v)) != cudaSuccess) return FA_ERR_CUDA;
+  return static_cast<fa_status>(v);
+}
+
+}  // extern "C"

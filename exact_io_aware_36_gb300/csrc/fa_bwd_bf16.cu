@@ -1,0 +1,578 @@
+// fa_bwd_bf16.cu -- tensor-core backward of exact attention for sm_103a.
+//
+// Method ("FlashAttention: Faster Attention Without Dropping a Single
+// Interaction", Key design 3): S and P are recomputed tile by tile from Q, K
+// and the saved LSE; D_i = dO_i . O_i replaces the row reduction of P o dP;
+// dS = P o (dP - D); dV += P^T dO, dK += dS^T Q, dQ += dS K.  The scale
+// factor of S enters dK and dQ once more (chain rule) and is applied at the
+// end.
+//
+// Three kernels on the caller's stream:
+//   preprocess  D = rowsum(dO o O) in fp32 ([Hq, T]) and dQacc = 0
+//               ([Hq, T, d] fp32, head-major so a query tile is contiguous).
+//   dkdv        one CTA per (key tile of 128, kv head, sequence): loops over
+//               the query heads of the kv head's group and over query tiles
+//               of 64 (causal: only tiles at or after the key tile), keeping
+//               dK and dV in TMEM; each step's dQ contribution is added to
+//               dQacc with a bulk fp32 reduction from shared memory.
+//   dq_convert  dQ = scale * dQacc -> bf16 [T, Hq, d].
+//
+// dkdv roles (320 threads):
+//   warps 0-3  "compute": one TMEM lane = one key row; recompute
+//              P^T = 2^(S^T * scale * log2 e + bias - L2) and
+//              dS^T = P^T o (dP^T - D); P^T and dS^T go back to TMEM (bf16)
+//              as A operands and dS^T also to shared memory (swizzled) as
+//              the B operand of dQ^T.
+//   warps 4-7  dQ drain: dQ^T rows (one TMEM lane = one head-dim column)
+//              to shared memory, then one bulk reduce-add into dQacc.
+//   warp 8     MMA issuer; warp 9 TMA producer (K, V once; Q, dO per step
+//              into 3 stages, with that step's L2 = LSE * log2 e and D).
+// MMAs per step i (M = 128 keys; queries N = 64):
+//   S^T(i) = K Q_i^T and dP^T(i) = V dO_i^T          (SS, both K-major)
+//   dV += P^T(i) dO_i and dK += dS^T(i) Q_i           (TS, B MN-major)
+//   dQ^T(i) = K^T dS^T(i)                             (SS, A and B MN-major)
+// TMEM: dV [0,d), dK [d,2d), S^T buffers at 256/320, dP^T buffers at
+// 384/448 (64 columns each, double buffered); dQ^T(i) reuses the dP^T
+// buffer of step i once dK(i) has read dS^T(i) from it.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa_host_util.h"
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr int kQStages = 3;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int NB = D / 64;
+  static constexpr int KV_BOX = 128 * 64 * 2;     // 128 rows x 64 columns
+  static constexpr int KV_TILE = NB * KV_BOX;
+  static constexpr int Q_BOX = 64 * 64 * 2;       // 64 rows x 64 columns
+  static constexpr int Q_TILE = NB * Q_BOX;
+  static constexpr int DS_BYTES = 128 * 64 * 2;   // dS^T: 128 keys x 64 queries
+  static constexpr int DQ_BYTES = 64 * D * 4;     // fp32 dQ staging, [64][D]
+  static constexpr int SIDE_BYTES = 528;          // L2[64], D[64], slope
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = K_OFF + KV_TILE;
+  static constexpr int Q_OFF = V_OFF + KV_TILE;
+  static constexpr int DO_OFF = Q_OFF + kQStages * Q_TILE;
+  static constexpr int DS_OFF = DO_OFF + kQStages * Q_TILE;
+  static constexpr int DQ_OFF = DS_OFF + 2 * DS_BYTES;
+  static constexpr int SIDE_OFF = DQ_OFF + DQ_BYTES;
+  static constexpr int BAR_OFF = SIDE_OFF + kQStages * SIDE_BYTES;
+  static constexpr int SMEM_BYTES = BAR_OFF + 128 + 1024;
+  static constexpr uint32_t DV_COL = 0, DK_COL = D;
+  static constexpr uint32_t SB_COL0 = 256, PB_COL0 = 384;   // + 64 * buffer
+};
+
+struct BwdBars {
+  uint64_t kv_full;
+  uint64_t q_full[kQStages], q_empty[kQStages];
+  uint64_t sdp_full[2];
+  uint64_t p_ready, dq_full, dq_free, dqs_free, dqs_full, dkdv_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(BwdBars) <= 128, "barrier block");
+
+struct Side {
+  float L2[64];
+  float Dv[64];
+  float slope2;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ bool seq_bounds(const AttnParams& p, int b, long long* seq0, int* L) {
+  if (p.cu_seqlens) {
+    const int c0 = __ldg(p.cu_seqlens + b);
+    const int c1 = __ldg(p.cu_seqlens + b + 1);
+    if ((b == 0 && c0 != 0) || c1 < c0 || (long long)c1 > p.T || c1 - c0 > p.N) return false;
+    *seq0 = c0;
+    *L = c1 - c0;
+  } else {
+    *seq0 = (long long)b * p.N;
+    *L = p.N;
+  }
+  return true;
+}
+
+// ----------------------------------------------------------------- preprocess
+// One warp per (token, query head): D = dO . O in fp32, and the dQ
+// accumulator row zeroed.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const AttnParams p) {
+  const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (w >= p.T * p.Hq) return;
+  const long long t = w / p.Hq;
+  const int h = (int)(w - t * p.Hq);
+  const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(p.dO) + (t * p.Hq + h) * D;
+  constexpr int PER = D / 32;   // elements per lane: 2 or 4
+  float o_v[PER], g_v[PER];
+  if (PER == 4) {
+    const uint2 bb = reinterpret_cast<const uint2*>(g)[lane];
+    const float2 y0 = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(&bb)[0]);
+    const float2 y1 = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(&bb)[1]);
+    g_v[0] = y0.x; g_v[1] = y0.y; g_v[2 % PER] = y1.x; g_v[3 % PER] = y1.y;
+  } else {
+    const float2 y = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(g)[lane]);
+    g_v[0] = y.x; g_v[1 % PER] = y.y;
+  }
+  if (p.o_f32) {
+    const float* o = static_cast<const float*>(p.o) + (t * p.Hq + h) * D + lane * PER;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) o_v[i] = o[i];
+  } else {
+    const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(p.o) + (t * p.Hq + h) * D + lane * PER;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) o_v[i] = __bfloat162float(o[i]);
+  }
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc = fmaf(o_v[i], g_v[i], acc);
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (lane == 0) p.D[(long long)h * p.T + t] = acc;
+  float4* z = reinterpret_cast<float4*>(p.dq_acc + ((long long)h * p.T + t) * D);
+  if (lane < D / 4) z[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// ----------------------------------------------------------------- dq convert
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const AttnParams p) {
+  const long long e = (long long)blockIdx.x * 256 + threadIdx.x;   // one per 8 outputs
+  const long long total = p.T * p.Hq * (D / 8);
+  if (e >= total) return;
+  const int c8 = (int)(e % (D / 8));
+  const long long th = e / (D / 8);
+  const long long t = th / p.Hq;
+  const int h = (int)(th - t * p.Hq);
+  const float4* src = reinterpret_cast<const float4*>(p.dq_acc + ((long long)h * p.T + t) * D + c8 * 8);
+  const float4 a = src[0], b = src[1];
+  const float s = p.scale;
+  uint4 out;
+  out.x = pack_bf16x2(a.x * s, a.y * s);
+  out.y = pack_bf16x2(a.z * s, a.w * s);
+  out.z = pack_bf16x2(b.x * s, b.y * s);
+  out.w = pack_bf16x2(b.z * s, b.w * s);
+  reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dq) + (t * p.Hq + h) * D + c8 * 8)[0] = out;
+}
+
+// ---------------------------------------------------------------------- dkdv
+template <int D, bool CAUSAL, bool ALIBI>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                const AttnParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::BAR_OFF);
+  Side* side = reinterpret_cast<Side*>(smem + C::SIDE_OFF);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.z;
+  const int g = blockIdx.y;                 // kv head
+  const int n0 = blockIdx.x * 128;          // key tile start within the sequence
+  long long seq0;
+  int L;
+  if (!seq_bounds(p, b, &seq0, &L)) {
+    if (threadIdx.x == 0) record_status(p.status, FA_ERR_CU_SEQLENS);
+    return;
+  }
+  if (n0 >= L) return;
+  const int nqt_all = (L + 63) / 64;
+  const int qt0 = CAUSAL ? n0 / 64 : 0;
+  const int nqt = nqt_all - qt0;            // query tiles per head (>= 1)
+  const int n_iter = p.group * nqt;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    for (int s = 0; s < kQStages; ++s) {
+      mbar_init(&bars->q_full[s], 33);
+      mbar_init(&bars->q_empty[s], 1);
+    }
+    mbar_init(&bars->sdp_full[0], 1);
+    mbar_init(&bars->sdp_full[1], 1);
+    mbar_init(&bars->p_ready, 4);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_free, 4);
+    mbar_init(&bars->dqs_free, 1);
+    mbar_init(&bars->dqs_full, 4);
+    mbar_init(&bars->dkdv_done, 1);
+    bars->abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const WaitCtx wc{&bars->abort_flag, p.status};
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmdO);
+      mbar_arrive_expect_tx(&bars->kv_full, 2 * C::KV_TILE);
+#pragma unroll
+      for (int bx = 0; bx < C::NB; ++bx) {
+        tma_load_3d(smem + C::K_OFF + bx * C::KV_BOX, &tmK, bx * 64, g, (int)(seq0 + n0), &bars->kv_full);
+        tma_load_3d(smem + C::V_OFF + bx * C::KV_BOX, &tmV, bx * 64, g, (int)(seq0 + n0), &bars->kv_full);
+      }
+    }
+    __syncwarp();
+    int issued = 0;
+    for (int it = 0; it < n_iter; ++it) {
+      const int st = it % kQStages;
+      if (!wait_warp(&bars->q_empty[st], ((it / kQStages) & 1) ^ 1, wc)) break;
+      const int h = g * p.group + it / nqt;
+      const int q0 = (qt0 + it % nqt) * 64;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->q_full[st], 2 * C::Q_TILE);
+#pragma unroll
+        for (int bx = 0; bx < C::NB; ++bx) {
+          tma_load_3d(smem + C::Q_OFF + st * C::Q_TILE + bx * C::Q_BOX, &tmQ, bx * 64, h,
+                      (int)(seq0 + q0), &bars->q_full[st]);
+          tma_load_3d(smem + C::DO_OFF + st * C::Q_TILE + bx * C::Q_BOX, &tmdO, bx * 64, h,
+                      (int)(seq0 + q0), &bars->q_full[st]);
+        }
+      }
+      Side* sd = side + st;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int qq = lane + 32 * r;
+        const bool valid = q0 + qq < L;
+        const long long idx = (long long)h * p.T + seq0 + q0 + qq;
+        sd->L2[qq] = valid ? __ldg(p.lse + idx) * kLog2e : INFINITY;
+        sd->Dv[qq] = valid ? __ldg(p.D + idx) : 0.f;
+      }
+      if (lane == 0) sd->slope2 = ALIBI ? __ldg(p.alibi + h) * kLog2e : 0.f;
+      __syncwarp();
+      mbar_arrive(&bars->q_full[st]);
+      issued = it + 1;
+    }
+    wait_warp_drain(&bars->kv_full, 0);
+    for (int it = max(0, issued - kQStages); it < issued; ++it)
+      wait_warp_drain(&bars->q_full[it % kQStages], (it / kQStages) & 1);
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    constexpr uint32_t ID_S = idesc_bf16_f32(128, 64, 0, 0);   // S^T, dP^T
+    constexpr uint32_t ID_KV = idesc_bf16_f32(128, D, 0, 1);   // dV, dK (A from TMEM)
+    constexpr uint32_t ID_DQ = idesc_bf16_f32(128, 64, 1, 1);  // dQ^T
+    const uint32_t sK = smem_u32(smem + C::K_OFF);
+    const uint32_t sV = smem_u32(smem + C::V_OFF);
+    const uint32_t sQ = smem_u32(smem + C::Q_OFF);
+    const uint32_t sdO = smem_u32(smem + C::DO_OFF);
+    const uint32_t sdS = smem_u32(smem + C::DS_OFF);
+
+    // S^T(i) into buffer i%2 and dP^T(i) into buffer i%2 (dP waits for the
+    // dQ drain of step i-2, which used the same columns).
+    auto issue_s = [&](int i) {
+      const int st = i % kQStages;
+      const uint32_t qb = sQ + st * C::Q_TILE;
+      const uint32_t dcol = C::SB_COL0 + 64 * (i & 1);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t offk = (kk >> 2) * C::KV_BOX + (kk & 3) * 32;
+        const uint32_t offq = (kk >> 2) * C::Q_BOX + (kk & 3) * 32;
+        mma_ss(tmem + dcol, smem_desc_sw128(sK + offk, 16, 1024), smem_desc_sw128(qb + offq, 16, 1024),
+               ID_S, kk > 0 ? 1u : 0u);
+      }
+    };
+    auto issue_dp = [&](int i) {
+      const int st = i % kQStages;
+      const uint32_t ob = sdO + st * C::Q_TILE;
+      const uint32_t dcol = C::PB_COL0 + 64 * (i & 1);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t offk = (kk >> 2) * C::KV_BOX + (kk & 3) * 32;
+        const uint32_t offq = (kk >> 2) * C::Q_BOX + (kk & 3) * 32;
+        mma_ss(tmem + dcol, smem_desc_sw128(sV + offk, 16, 1024), smem_desc_sw128(ob + offq, 16, 1024),
+               ID_S, kk > 0 ? 1u : 0u);
+      }
+    };
+
+    bool ok = wait_warp(&bars->kv_full, 0, wc);
+    for (int i = 0; ok && i < 2 && i < n_iter; ++i) {
+      if (!(ok = wait_warp(&bars->q_full[i % kQStages], (i / kQStages) & 1, wc))) break;
+      tc_fence_after();
+      if (lane == 0) {
+        issue_s(i);
+        issue_dp(i);
+        mma_commit(&bars->sdp_full[i & 1]);
+      }
+      __syncwarp();
+    }
+    for (int it = 0; ok && it < n_iter; ++it) {
+      const int st = it % kQStages;
+      const int buf = it & 1;
+      if (!(ok = wait_warp(&bars->p_ready, it & 1, wc))) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t ob = sdO + st * C::Q_TILE;
+        const uint32_t qb = sQ + st * C::Q_TILE;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)   // dV += P^T dO   (K = 64 queries)
+          mma_ts(tmem + C::DV_COL, tmem + C::SB_COL0 + 64 * buf + 8 * kk,
+                 smem_desc_sw128(ob + kk * 2048, C::Q_BOX, 1024), ID_KV, (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)   // dK += dS^T Q
+          mma_ts(tmem + C::DK_COL, tmem + C::PB_COL0 + 64 * buf + 8 * kk,
+                 smem_desc_sw128(qb + kk * 2048, C::Q_BOX, 1024), ID_KV, (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars->q_empty[st]);
+        const uint32_t dsb = sdS + buf * C::DS_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)   // dQ^T = K^T dS^T   (K = 128 keys)
+          mma_ss(tmem + C::PB_COL0 + 64 * buf, smem_desc_sw128(sK + kk * 2048, C::KV_BOX, 1024),
+                 smem_desc_sw128(dsb + kk * 2048, C::Q_BOX, 1024), ID_DQ, kk > 0 ? 1u : 0u);
+        mma_commit(&bars->dq_full);
+      }
+      __syncwarp();
+      const int nx = it + 2;
+      if (nx < n_iter) {
+        if (!(ok = wait_warp(&bars->q_full[nx % kQStages], (nx / kQStages) & 1, wc))) break;
+        tc_fence_after();
+        if (lane == 0) issue_s(nx);
+        __syncwarp();
+        if (!(ok = wait_warp(&bars->dq_free, it & 1, wc))) break;
+        tc_fence_after();
+        if (lane == 0) {
+          issue_dp(nx);
+          mma_commit(&bars->sdp_full[buf]);
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0) mma_commit(&bars->dkdv_done);
+    __syncwarp();
+    wait_warp_drain(&bars->dkdv_done, 0);
+  } else if (warp < 4) {
+    // ------------------------------------------------------------- compute
+    const int kr = 32 * warp + lane;          // key row within the tile
+    const int key = n0 + kr;
+    const bool key_ok = key < L;
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+    const float c2 = p.scale_log2;
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      const int st = it % kQStages;
+      const int buf = it & 1;
+      const int q0 = (qt0 + it % nqt) * 64;
+      if (!(ok = wait_warp(&bars->sdp_full[buf], (it >> 1) & 1, wc))) break;
+      tc_fence_after();
+      const Side* sd = side + st;
+      const bool need_mask = (CAUSAL && q0 < n0 + 127) || !key_ok;
+      const float slope2 = ALIBI ? sd->slope2 : 0.f;
+      const float bias0 = ALIBI ? slope2 * (float)(key - q0) : 0.f;
+      uint8_t* dsrow = smem + C::DS_OFF + buf * C::DS_BYTES + kr * 128;
+      const uint32_t tSb = lane_base + C::SB_COL0 + 64 * buf;
+      const uint32_t tPb = lane_base + C::PB_COL0 + 64 * buf;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {    // 32 queries at a time
+        uint32_t sv[32], dp[32];
+        tmem_ld32(tSb + 32 * half, sv);
+        tmem_ld32(tPb + 32 * half, dp);
+        tmem_wait_ld();
+        reg_fence32(sv);
+        reg_fence32(dp);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          float pv[2], dv2[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int ql = 2 * c + e;            // query within the half
+            const int qq = 32 * half + ql;       // query within the tile
+            float x = __uint_as_float(sv[ql]) * c2;
+            if (ALIBI) x = fmaf(-slope2, (float)qq, x + bias0);
+            float pr = ex2_approx(x - sd->L2[qq]);
+            if (need_mask && (!key_ok || (CAUSAL && key > q0 + qq))) pr = 0.f;
+            pv[e] = pr;
+            dv2[e] = pr * (__uint_as_float(dp[ql]) - sd->Dv[qq]);
+          }
+          pk[c] = pack_bf16x2(pv[0], pv[1]);
+          dk[c] = pack_bf16x2(dv2[0], dv2[1]);
+        }
+        tmem_st16(tSb + 16 * half, pk);          // P^T (bf16) over consumed S^T columns
+        tmem_st16(tPb + 16 * half, dk);          // dS^T (bf16) over consumed dP^T columns
+#pragma unroll
+        for (int q16 = 0; q16 < 4; ++q16) {      // dS^T row into shared memory (swizzled)
+          const int chunk = 4 * half + q16;
+          const int phys = chunk ^ (kr & 7);
+          *reinterpret_cast<uint4*>(dsrow + phys * 16) =
+              make_uint4(dk[4 * q16], dk[4 * q16 + 1], dk[4 * q16 + 2], dk[4 * q16 + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_ready);
+    }
+    // dV epilogue
+    if (ok) ok = wait_warp(&bars->dkdv_done, 0, wc);
+    if (ok) {
+      tc_fence_after();
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.dv) + ((seq0 + key) * p.Hkv + g) * D;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(lane_base + C::DV_COL + c0, r);
+        tmem_wait_ld();
+        reg_fence32(r);
+        uint32_t pkd[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) pkd[c] = pack_bf16x2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]));
+        if (key_ok) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) d4[v4] = make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ drain
+    const int q4 = warp & 3;
+    const int c = 32 * q4 + lane;             // head-dim column of dQ^T
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * q4) << 16);
+    float* dqs = reinterpret_cast<float*>(smem + C::DQ_OFF);
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      const int buf = it & 1;
+      const int h = g * p.group + it / nqt;
+      const int q0 = (qt0 + it % nqt) * 64;
+      const int nvalid = min(64, L - q0);
+      if (!(ok = wait_warp(&bars->dq_full, it & 1, wc))) break;
+      tc_fence_after();
+      uint32_t r[64];
+      tmem_ld32(lane_base + C::PB_COL0 + 64 * buf, r);
+      tmem_ld32(lane_base + C::PB_COL0 + 64 * buf + 32, r + 32);
+      tmem_wait_ld();
+      reg_fence32(r);
+      reg_fence32(r + 32);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->dq_free);
+      if (!(ok = wait_warp(&bars->dqs_free, (it & 1) ^ 1, wc))) break;
+      if (c < D) {
+#pragma unroll
+        for (int qq = 0; qq < 64; ++qq) dqs[qq * D + c] = __uint_as_float(r[qq]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->dqs_full);
+      if (q4 == 0) {
+        if (!(ok = wait_warp(&bars->dqs_full, it & 1, wc))) break;
+        if (lane == 0) {
+          bulk_reduce_add_f32(p.dq_acc + ((long long)h * p.T + seq0 + q0) * D, dqs,
+                              (uint32_t)(nvalid * D * 4));
+          bulk_commit_group();
+          bulk_wait_group_read0();
+          mbar_arrive(&bars->dqs_free);
+        }
+        __syncwarp();
+      }
+    }
+    if (q4 == 0 && lane == 0) bulk_wait_group0();
+    __syncwarp();
+    // dK epilogue
+    if (ok) ok = wait_warp(&bars->dkdv_done, 0, wc);
+    if (ok) {
+      tc_fence_after();
+      const int key = n0 + c;
+      const bool key_ok = key < L;
+      const float sc = p.scale;
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.dk) + ((seq0 + key) * p.Hkv + g) * D;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(lane_base + C::DK_COL + c0, rr);
+        tmem_wait_ld();
+        reg_fence32(rr);
+        uint32_t pkd[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pkd[e] = pack_bf16x2(__uint_as_float(rr[2 * e]) * sc, __uint_as_float(rr[2 * e + 1]) * sc);
+        if (key_ok) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) d4[v4] = make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool CAUSAL, bool ALIBI>
+int launch_dkdv(const AttnParams& p, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  auto kern = bwd_dkdv_kernel<D, CAUSAL, ALIBI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return (int)e;
+  CUtensorMap tq, tk, tv, tdo;
+  int r = make_tmap_bf16_3d(&tq, p.q, D, p.Hq, p.T, 64);
+  if (!r) r = make_tmap_bf16_3d(&tdo, p.dO, D, p.Hq, p.T, 64);
+  if (!r) r = make_tmap_bf16_3d(&tk, p.k, D, p.Hkv, p.T, 128);
+  if (!r) r = make_tmap_bf16_3d(&tv, p.v, D, p.Hkv, p.T, 128);
+  if (r) return r;
+  dim3 grid((p.N + 127) / 128, p.Hkv, p.B);
+  kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, p);
+  return (int)cudaGetLastError();
+}
+
+template <int D>
+int launch_stages(const AttnParams& p, cudaStream_t stream, int stage) {
+  const long long rows = p.T * p.Hq;
+  if (stage < 0 || stage == 0) {
+    bwd_preprocess_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return (int)e;
+  }
+  if (stage < 0 || stage == 1) {
+    int r;
+    const bool alibi = p.alibi != nullptr;
+    if (p.causal) r = alibi ? launch_dkdv<D, true, true>(p, stream) : launch_dkdv<D, true, false>(p, stream);
+    else r = alibi ? launch_dkdv<D, false, true>(p, stream) : launch_dkdv<D, false, false>(p, stream);
+    if (r) return r;
+  }
+  if (stage < 0 || stage == 2) {
+    const long long n8 = rows * (D / 8);
+    bwd_dq_convert_kernel<D><<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(p);
+    return (int)cudaGetLastError();
+  }
+  return 0;
+}
+
+}  // namespace
+
+int launch_bwd_bf16(const AttnParams& p, void* stream, int stage) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return p.d == 128 ? launch_stages<128>(p, s, stage) : launch_stages<64>(p, s, stage);
+}
+
+}  // namespace fa

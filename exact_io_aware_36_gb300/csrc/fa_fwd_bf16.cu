@@ -1,0 +1,422 @@
+// fa_fwd_bf16.cu -- tensor-core forward of exact attention for sm_103a.
+//
+// Method ("FlashAttention: Faster Attention Without Dropping a Single
+// Interaction"): Key design 1 (tiles of Q, K, V staged on chip; S and P never
+// leave the SM), Key design 2 (running max m and sum l merged tile by tile,
+// the output accumulator rescaled when m grows; FA2's L = m + log l saved per
+// row), Key design 4 (FA3-style asynchrony: producer and consumer roles).
+//
+// GB300 mapping (one CTA per SM, 320 threads, 2 query tiles of 128 rows):
+//   warp 9     TMA producer: Q0/Q1 once, then K_j and V_j into a ring of
+//              STAGES slots (128-byte swizzle), mbarrier full/empty pairs.
+//   warp 8     MMA issuer (one lane): S_t = Q_t K_j^T into TMEM (both
+//              operands K-major in shared memory), then O_t += P_t V_j with
+//              P_t read from TMEM and V_j MN-major in shared memory.
+//   warps 0-3  softmax of query tile 0 (one TMEM lane = one query row)
+//   warps 4-7  softmax of query tile 1
+// TMEM columns: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
+// P_t (bf16, two per 32-bit column) overwrites the first 64 columns of S_t.
+// The MMA stream per key tile j is PV0(j-1), S0(j), PV1(j-1), S1(j), so the
+// softmax of one tile overlaps the tensor work of the other.
+//
+// Softmax in base 2: x = s * scale * log2(e) (+ slope * log2(e) * (j - i)),
+// p = 2^(x - m_ref).  The reference max m_ref is only raised when a tile's
+// max exceeds it by more than kTau = 8 (lazy rescale): the result is the same
+// for any reference, and p stays <= 2^8.  When it is raised, the owning
+// thread rescales its O row in TMEM; this is safe then because the commit
+// that published S_t(j) also covers PV_t(j-1).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+#include "fa_host_util.h"
+
+namespace fa {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr float kTau = 8.0f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int NB = D / 64;                 // 64-column boxes per row
+  static constexpr int BOX_BYTES = 128 * 64 * 2;    // one 128 x 64 bf16 box
+  static constexpr int TILE_BYTES = NB * BOX_BYTES; // one 128 x D tile
+  static constexpr int STAGES = D == 128 ? 2 : 4;
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = Q_OFF + 2 * TILE_BYTES;
+  static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
+  static constexpr int BAR_OFF = V_OFF + STAGES * TILE_BYTES;
+  static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
+  static constexpr uint32_t S_COL0 = 0, S_COL1 = 128;
+  static constexpr uint32_t O_COL0 = 256, O_COL1 = 256 + D;
+};
+
+struct FwdBars {
+  uint64_t q_full;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full[2], p_full[2];
+  uint64_t o_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+template <int D, bool CAUSAL, bool ALIBI>
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  FwdBars* bars = reinterpret_cast<FwdBars*>(smem + C::BAR_OFF);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.z;
+  const int h = blockIdx.y;
+  const int qb = CAUSAL ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+
+  long long seq0;
+  int L;
+  if (p.cu_seqlens) {
+    const int c0 = __ldg(p.cu_seqlens + b);
+    const int c1 = __ldg(p.cu_seqlens + b + 1);
+    if ((b == 0 && c0 != 0) || c1 < c0 || (long long)c1 > p.T || c1 - c0 > p.N) {
+      if (threadIdx.x == 0) record_status(p.status, FA_ERR_CU_SEQLENS);
+      return;
+    }
+    seq0 = c0;
+    L = c1 - c0;
+  } else {
+    seq0 = (long long)b * p.N;
+    L = p.N;
+  }
+  const int m0 = qb * 256;
+  if (m0 >= L) return;                       // uniform: nothing to do
+  const bool tile1 = m0 + 128 < L;
+  int nkv[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int rows_end = min(m0 + 128 * (t + 1), L);
+    nkv[t] = CAUSAL ? (rows_end + 127) / 128 : (L + 127) / 128;
+  }
+  if (!tile1) nkv[1] = 0;
+  const int nkv_max = max(nkv[0], nkv[1]);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], 4);
+    }
+    mbar_init(&bars->o_done, 1);
+    bars->abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const WaitCtx wc{&bars->abort_flag, p.status};
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ producer
+    const int kvh = h / p.group;
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const int ntiles = tile1 ? 2 : 1;
+      mbar_arrive_expect_tx(&bars->q_full, ntiles * C::TILE_BYTES);
+      for (int t = 0; t < ntiles; ++t)
+#pragma unroll
+        for (int bx = 0; bx < C::NB; ++bx)
+          tma_load_3d(smem + C::Q_OFF + t * C::TILE_BYTES + bx * C::BOX_BYTES, &tmQ, bx * 64, h,
+                      (int)(seq0 + m0 + 128 * t), &bars->q_full);
+    }
+    __syncwarp();
+    int issued = 0;                 // K/V tiles whose loads were issued
+    for (int j = 0; j < nkv_max; ++j) {
+      const int s = j % C::STAGES;
+      const uint32_t ph = ((j / C::STAGES) & 1) ^ 1;
+      if (!wait_warp(&bars->k_empty[s], ph, wc)) break;
+      if (!wait_warp(&bars->v_empty[s], ph, wc)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->k_full[s], C::TILE_BYTES);
+#pragma unroll
+        for (int bx = 0; bx < C::NB; ++bx)
+          tma_load_3d(smem + C::K_OFF + s * C::TILE_BYTES + bx * C::BOX_BYTES, &tmK, bx * 64, kvh,
+                      (int)(seq0 + 128 * j), &bars->k_full[s]);
+        mbar_arrive_expect_tx(&bars->v_full[s], C::TILE_BYTES);
+#pragma unroll
+        for (int bx = 0; bx < C::NB; ++bx)
+          tma_load_3d(smem + C::V_OFF + s * C::TILE_BYTES + bx * C::BOX_BYTES, &tmV, bx * 64, kvh,
+                      (int)(seq0 + 128 * j), &bars->v_full[s]);
+      }
+      __syncwarp();
+      issued = j + 1;
+    }
+    // Loads in flight must land before this CTA's shared memory goes away.
+    wait_warp_drain(&bars->q_full, 0);
+    for (int j = max(0, issued - C::STAGES); j < issued; ++j) {
+      const int s = j % C::STAGES;
+      const uint32_t ph = (j / C::STAGES) & 1;
+      wait_warp_drain(&bars->k_full[s], ph);
+      wait_warp_drain(&bars->v_full[s], ph);
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);
+    constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);
+    const uint32_t sQ = smem_u32(smem + C::Q_OFF);
+    const uint32_t sK = smem_u32(smem + C::K_OFF);
+    const uint32_t sV = smem_u32(smem + C::V_OFF);
+    const uint32_t colS[2] = {C::S_COL0, C::S_COL1};
+    const uint32_t colO[2] = {C::O_COL0, C::O_COL1};
+    bool ok = wait_warp(&bars->q_full, 0, wc);
+    for (int j = 0; ok && j <= nkv_max; ++j) {
+      const int sj = j % C::STAGES;
+      const int sp = (j + C::STAGES - 1) % C::STAGES;
+      if (j < nkv_max && !(ok = wait_warp(&bars->k_full[sj], (j / C::STAGES) & 1, wc))) break;
+      if (j >= 1 && !(ok = wait_warp(&bars->v_full[sp], ((j - 1) / C::STAGES) & 1, wc))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (j >= 1 && j - 1 < nkv[t]) {
+          if (!(ok = wait_warp(&bars->p_full[t], (j - 1) & 1, wc))) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t vbase = sV + sp * C::TILE_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < 128 / 16; ++kk) {
+              const uint64_t bdesc = smem_desc_sw128(vbase + kk * 2048, C::BOX_BYTES, 1024);
+              mma_ts(tmem + colO[t], tmem + colS[t] + kk * 8, bdesc, IDESC_O,
+                     (j - 1 > 0 || kk > 0) ? 1u : 0u);
+            }
+          }
+          __syncwarp();
+        }
+        if (j < nkv[t]) {
+          if (lane == 0) {
+            const uint32_t qbase = sQ + t * C::TILE_BYTES;
+            const uint32_t kbase = sK + sj * C::TILE_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
+              const uint64_t adesc = smem_desc_sw128(qbase + off, 16, 1024);
+              const uint64_t bdesc = smem_desc_sw128(kbase + off, 16, 1024);
+              mma_ss(tmem + colS[t], adesc, bdesc, IDESC_S, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&bars->s_full[t]);
+          }
+          __syncwarp();
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) {
+        if (j < nkv_max) mma_commit(&bars->k_empty[sj]);
+        if (j >= 1) mma_commit(&bars->v_empty[sp]);
+      }
+      __syncwarp();
+    }
+    if (lane == 0) mma_commit(&bars->o_done);
+    __syncwarp();
+    // Tensor-core work must be finished before the TMEM is released.
+    wait_warp_drain(&bars->o_done, 0);
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int t = warp >> 2;
+    const int q4 = warp & 3;
+    const int row = m0 + 128 * t + 32 * q4 + lane;       // row within the sequence
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * q4) << 16);
+    const uint32_t tS = lane_base + (t ? C::S_COL1 : C::S_COL0);
+    const uint32_t tO = lane_base + (t ? C::O_COL1 : C::O_COL0);
+    const float c2 = p.scale_log2;
+    float slope2 = 0.f;
+    if (ALIBI) slope2 = __ldg(p.alibi + h) * kLog2e;
+    float m_ref = -INFINITY;
+    float l = 0.f;     // sum of p in fp32: gives the LSE
+    float lr = 0.f;    // sum of the bf16-rounded p the PV MMA sees: normalises O
+    bool ok = true;
+    for (int j = 0; j < nkv[t]; ++j) {
+      if (!(ok = wait_warp(&bars->s_full[t], j & 1, wc))) break;
+      tc_fence_after();
+      uint32_t s[128];
+      tmem_ld32(tS + 0, s);
+      tmem_ld32(tS + 32, s + 32);
+      tmem_ld32(tS + 64, s + 64);
+      tmem_ld32(tS + 96, s + 96);
+      tmem_wait_ld();
+      reg_fence32(s);
+      reg_fence32(s + 32);
+      reg_fence32(s + 64);
+      reg_fence32(s + 96);
+      const int n0 = 128 * j;
+      const bool need_mask = (CAUSAL && n0 + 127 > m0 + 128 * t) || (n0 + 128 > L);
+      float xmax = -INFINITY;
+      if (ALIBI) {
+        const float base = slope2 * (float)(n0 - row);
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          float x = fmaf(__uint_as_float(s[c]), c2, fmaf(slope2, (float)c, base));
+          if (need_mask) {
+            const int key = n0 + c;
+            if (key >= L || (CAUSAL && key > row)) x = -INFINITY;
+          }
+          s[c] = __float_as_uint(x);
+          xmax = fmaxf(xmax, x);
+        }
+      } else {
+        if (need_mask) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            const int key = n0 + c;
+            if (key >= L || (CAUSAL && key > row)) s[c] = __float_as_uint(-INFINITY);
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 128; ++c) xmax = fmaxf(xmax, __uint_as_float(s[c]));
+        xmax *= c2;
+      }
+      // lazy rescale: raise the reference only when the max grew past tau
+      const bool raise = xmax > m_ref + kTau;
+      const float m_new = raise ? xmax : m_ref;
+      const float alpha = raise ? ex2_approx(m_ref - m_new) : 1.f;
+      l *= alpha;
+      lr *= alpha;
+      if (j > 0 && __any_sync(0xffffffffu, raise)) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          uint32_t o[16];
+          tmem_ld16(tO + c0, o);
+          tmem_wait_ld();
+          reg_fence16(o);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+          tmem_st16(tO + c0, o);
+        }
+      }
+      m_ref = m_new;
+      const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
+      float rs = 0.f, rsr = 0.f;
+      // P in chunks of 32 scores -> 16 packed columns, stored as produced
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float x0 = __uint_as_float(s[32 * ch + 2 * c]);
+          const float x1 = __uint_as_float(s[32 * ch + 2 * c + 1]);
+          const float p0 = ALIBI ? ex2_approx(x0 - mb) : ex2_approx(fmaf(x0, c2, -mb));
+          const float p1 = ALIBI ? ex2_approx(x1 - mb) : ex2_approx(fmaf(x1, c2, -mb));
+          rs += p0 + p1;
+          pk[c] = pack_bf16x2(p0, p1);
+          rsr += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xFFFF0000u);
+        }
+        tmem_st16(tS + 16 * ch, pk);
+      }
+      l += rs;
+      lr += rsr;
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full[t]);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && nkv[t] > 0) ok = wait_warp(&bars->o_done, 0, wc);
+    if (ok && nkv[t] > 0) {
+      tc_fence_after();
+      const bool valid = row < L;
+      const float inv = lr > 0.f ? 1.f / lr : 0.f;
+      const long long tok = seq0 + row;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(tO + c0, o);
+        tmem_wait_ld();
+        reg_fence32(o);
+        if (p.o_f32) {
+          float* O = static_cast<float*>(p.o) + (tok * p.Hq + h) * D + c0;
+          if (valid) {
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+              reinterpret_cast<float4*>(O)[v4] =
+                  make_float4(__uint_as_float(o[4 * v4]) * inv, __uint_as_float(o[4 * v4 + 1]) * inv,
+                              __uint_as_float(o[4 * v4 + 2]) * inv, __uint_as_float(o[4 * v4 + 3]) * inv);
+          }
+        } else {
+          __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o) + (tok * p.Hq + h) * D + c0;
+          uint32_t pkd[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            pkd[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
+          if (valid) {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              reinterpret_cast<uint4*>(O)[v4] =
+                  make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
+          }
+        }
+      }
+      if (valid)
+        p.lse[(long long)h * p.T + tok] = l > 0.f ? (m_ref + lg2_approx(l)) * kLn2 : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool CAUSAL, bool ALIBI>
+int launch_impl(const AttnParams& p, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  auto kern = fwd_bf16_kernel<D, CAUSAL, ALIBI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_BYTES);
+  if (e != cudaSuccess) return (int)e;
+  CUtensorMap tq, tk, tv;
+  int r = make_tmap_bf16_3d(&tq, p.q, D, p.Hq, p.T, 128);
+  if (!r) r = make_tmap_bf16_3d(&tk, p.k, D, p.Hkv, p.T, 128);
+  if (!r) r = make_tmap_bf16_3d(&tv, p.v, D, p.Hkv, p.T, 128);
+  if (r) return r;
+  dim3 grid((p.N + 255) / 256, p.Hq, p.B);
+  kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace
+
+int launch_fwd_bf16(const AttnParams& p, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  const bool alibi = p.alibi != nullptr;
+  if (p.d == 128) {
+    if (p.causal) return alibi ? launch_impl<128, true, true>(p, stream) : launch_impl<128, true, false>(p, stream);
+    return alibi ? launch_impl<128, false, true>(p, stream) : launch_impl<128, false, false>(p, stream);
+  }
+  if (p.causal) return alibi ? launch_impl<64, true, true>(p, stream) : launch_impl<64, true, false>(p, stream);
+  return alibi ? launch_impl<64, false, true>(p, stream) : launch_impl<64, false, false>(p, stream);
+}
+
+}  // namespace fa

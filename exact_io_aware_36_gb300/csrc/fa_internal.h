@@ -1,0 +1,47 @@
+// fa_internal.h -- parameters shared by the host library and its kernels.
+#pragma once
+#include <stdint.h>
+
+#include "../../include/fa.h"
+
+namespace fa {
+
+// Limit of every pipeline wait inside a kernel (wall clock, nanoseconds).
+// A healthy wait lasts microseconds; the limit only turns a lost arrival
+// into an error status instead of a hung GPU.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// log2(e): scores are moved to the base-2 domain so the softmax uses exp2.
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct AttnParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  const void* dO;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* D;          // workspace: D_i = dO_i . O_i, [Hq, T]
+  float* dq_acc;     // workspace: fp32 dQ accumulator, [Hq, T, d]
+  const int32_t* cu_seqlens;   // [B+1] or nullptr
+  const float* alibi;          // [Hq] or nullptr
+  unsigned int* status;        // per-device status word
+  long long T;
+  int B, Hq, Hkv, N, d;
+  int group;                   // Hq / Hkv
+  int causal;
+  int o_f32;                    // o stored as fp32 (else the input dtype)
+  float scale;
+  float scale_log2;            // scale * log2(e)
+};
+
+// Launchers (each returns a cudaError_t value as int).
+int launch_fwd_fp32(const AttnParams& p, void* stream);
+int launch_fwd_bf16(const AttnParams& p, void* stream);
+int launch_bwd_bf16(const AttnParams& p, void* stream, int stage);   // stage < 0: all
+
+}  // namespace fa

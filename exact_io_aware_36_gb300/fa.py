@@ -1,0 +1,205 @@
+"""Thin ctypes binding of libfa (include/fa.h).
+
+Only argument marshalling happens here: torch tensors become device pointers
+and the current CUDA stream becomes a ``cudaStream_t``.  Every step of the
+attention computation runs in the library's CUDA kernels.  There is no other
+implementation behind these functions: if the library is missing or fails
+to load, the calls raise.
+
+Raw entry points with the C names (``fa_fwd``, ``fa_bwd``,
+``fa_bwd_workspace_size``, ``fa_check_device_error``, ``fa_status_string``)
+take integer pointers; ``attention_forward`` / ``attention_backward`` take
+torch tensors and allocate the outputs with torch.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libfa.so")
+
+FA_BF16, FA_FP32 = 0, 1
+STATUS = {
+    0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_SHAPE", 3: "FA_ERR_UNSUPPORTED", 4: "FA_ERR_ALIGN",
+    5: "FA_ERR_WORKSPACE", 6: "FA_ERR_CUDA", 7: "FA_ERR_DEVICE_TIMEOUT", 8: "FA_ERR_CU_SEQLENS",
+}
+EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_stage", "fa_bwd_workspace_size", "fa_check_device_error",
+           "fa_status_string", "fa_version")
+FA_BWD_PREPROCESS, FA_BWD_DKDV, FA_BWD_DQ_CONVERT = 0, 1, 2
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        name = STATUS.get(status, str(status))
+        msg = f"{what}: {name}" if what else name
+        try:
+            msg += f" ({fa_status_string(status)})"
+        except Exception:
+            pass
+        super().__init__(msg)
+
+
+_lib = None
+
+
+def load(path: Optional[str] = None):
+    """Load libfa (once) and declare the C signatures."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise FAError(6, f"libfa not built ({p} missing); run exact_io_aware_36_gb300.build")
+    lib = ctypes.CDLL(p)
+    vp, i, f, ll, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong, ctypes.c_size_t
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, ll, vp, i, i, vp]
+    lib.fa_fwd.restype = i
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, ll, vp, i,
+                           i, vp, sz, vp]
+    lib.fa_bwd.restype = i
+    lib.fa_bwd_stage.argtypes = [i] + lib.fa_bwd.argtypes
+    lib.fa_bwd_stage.restype = i
+    lib.fa_bwd_workspace_size.argtypes = [i, i, i, i, ll]
+    lib.fa_bwd_workspace_size.restype = sz
+    lib.fa_check_device_error.argtypes = [vp]
+    lib.fa_check_device_error.restype = i
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_version.argtypes = []
+    lib.fa_version.restype = i
+    if path is None:
+        _lib = lib
+    return lib
+
+
+# ------------------------------------------------------------ raw C entry points
+
+def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, cu_seqlens, total_tokens,
+           alibi_slopes, dtype, o_dtype, stream) -> int:
+    return load().fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, int(causal), cu_seqlens,
+                         total_tokens, alibi_slopes, dtype, o_dtype, stream)
+
+
+def fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal, cu_seqlens,
+           total_tokens, alibi_slopes, dtype, o_dtype, workspace, workspace_bytes, stream) -> int:
+    return load().fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, int(causal),
+                         cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype, workspace,
+                         workspace_bytes, stream)
+
+
+def fa_bwd_stage(stage, q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal,
+                 cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype, workspace,
+                 workspace_bytes, stream) -> int:
+    return load().fa_bwd_stage(stage, q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale,
+                               int(causal), cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype,
+                               workspace, workspace_bytes, stream)
+
+
+def fa_bwd_workspace_size(B, Hq, N, d, total_tokens) -> int:
+    return load().fa_bwd_workspace_size(B, Hq, N, d, total_tokens)
+
+
+def fa_check_device_error(stream=None) -> int:
+    return load().fa_check_device_error(stream)
+
+
+def fa_status_string(status: int) -> str:
+    return load().fa_status_string(status).decode()
+
+
+# ------------------------------------------------------------ torch wrappers
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise FAError(status, what)
+
+
+def _sizes(q, k, cu_seqlens, max_seqlen, batch):
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    if cu_seqlens is not None:
+        B = cu_seqlens.numel() - 1
+        if max_seqlen is None:
+            raise ValueError("max_seqlen is required with cu_seqlens")
+        N = int(max_seqlen)
+    else:
+        B = int(batch) if batch is not None else 1
+        N = T // B if B else 0
+    return T, B, Hq, Hkv, N, d
+
+
+def _dtype_code(dt):
+    import torch
+    return FA_BF16 if dt == torch.bfloat16 else FA_FP32 if dt == torch.float32 else -1
+
+
+def attention_forward(q, k, v, *, causal: bool, scale: Optional[float] = None, cu_seqlens=None,
+                      max_seqlen: Optional[int] = None, batch: Optional[int] = None,
+                      alibi_slopes=None, out=None, lse=None, out_dtype=None, stream=None,
+                      check: bool = False):
+    """O, LSE = attention(q, k, v) through ``fa_fwd``.
+
+    q: [T, Hq, d], k/v: [T, Hkv, d] (bf16 or fp32, contiguous, on the GPU).
+    Dense batches pass ``batch`` (T = batch * N); packed batches pass int32
+    ``cu_seqlens`` [B+1] and ``max_seqlen``.  Returns (o [T, Hq, d] of
+    ``out_dtype`` (default: ``out``'s dtype, else q's), lse float32 [Hq, T]).
+    """
+    import torch
+    T, B, Hq, Hkv, N, d = _sizes(q, k, cu_seqlens, max_seqlen, batch)
+    dtype = _dtype_code(q.dtype)
+    if dtype < 0:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype or q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
+    st = fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, N, d, float(scale),
+                causal, _ptr(cu_seqlens), T, _ptr(alibi_slopes), dtype, _dtype_code(out.dtype),
+                _stream(stream))
+    _check(st, "fa_fwd")
+    if check:
+        _check(fa_check_device_error(_stream(stream)), "fa_fwd (device)")
+    return out, lse
+
+
+def attention_backward(q, k, v, o, dO, lse, *, causal: bool, scale: Optional[float] = None,
+                       cu_seqlens=None, max_seqlen: Optional[int] = None,
+                       batch: Optional[int] = None, alibi_slopes=None, workspace=None,
+                       dq=None, dk=None, dv=None, stream=None, check: bool = False):
+    """dQ, dK, dV through ``fa_bwd`` (bf16).  ``workspace`` (uint8 device
+    tensor of at least ``fa_bwd_workspace_size`` bytes) is allocated when
+    not given."""
+    import torch
+    T, B, Hq, Hkv, N, d = _sizes(q, k, cu_seqlens, max_seqlen, batch)
+    if q.dtype != torch.bfloat16:
+        raise TypeError("fa_bwd takes bf16 tensors")
+    if scale is None:
+        scale = d ** -0.5
+    need = fa_bwd_workspace_size(B, Hq, N, d, T)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    st = fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk),
+                _ptr(dv), B, Hq, Hkv, N, d, float(scale), causal, _ptr(cu_seqlens), T,
+                _ptr(alibi_slopes), FA_BF16, _dtype_code(o.dtype), _ptr(workspace),
+                workspace.numel(), _stream(stream))
+    _check(st, "fa_bwd")
+    if check:
+        _check(fa_check_device_error(_stream(stream)), "fa_bwd (device)")
+    return dq, dk, dv

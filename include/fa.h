@@ -1,0 +1,160 @@
+/*
+ * fa.h -- C ABI of libfa: exact IO-aware scaled-dot-product attention on one
+ * NVIDIA GB300 (sm_103a), forward and backward.
+ *
+ * What it computes.  For each sequence b and query head h, with kv head
+ * g = h / (Hq / Hkv) and positions i (query) and j (key) local to the
+ * sequence:
+ *     S = scale * Q K^T + B_h,   P = softmax(S) row-wise,   O = P V,
+ *     LSE_i = log sum_j exp(S_ij)                         (natural log)
+ * ("FlashAttention: Faster Attention Without Dropping a Single Interaction",
+ * Key design 1, the S/P/O definition; Key design 2, the saved statistic
+ * L = m + log l).  B_h[i,j] = -slope_h * (i - j) when ALiBi slopes are given,
+ * else 0; with causal != 0, S_ij = -inf for j > i.  The bias is added after
+ * scaling and is not scaled.
+ * The backward recomputes P from LSE tile by tile (Key design 3):
+ *     dV = P^T dO,  dP = dO V^T,  D_i = dO_i . O_i,  dS = P o (dP - D),
+ *     dQ = scale * dS K,  dK = scale * dS^T Q,
+ * with dK and dV of kv head g summed over the query heads of its group.
+ * S and P are never written to device memory.
+ *
+ * Layouts (all row-major and contiguous; q, k, v, dO, dq, dk, dv have the
+ * element type `dtype`, o has `o_dtype`):
+ *     q, o, dO, dq : [T, Hq,  d]
+ *     k, v, dk, dv : [T, Hkv, d]
+ *     lse          : float32 [Hq, T]
+ * where T is the total token count.  Dense batches: cu_seqlens == NULL, the
+ * B sequences of length N are stored back to back, T = B * N.  Packed
+ * ("varlen") batches ("FlashAttention: The Algorithm That Beat the Memory
+ * Wall", "Varlen Is the Quiet Superpower"): cu_seqlens is a device int32
+ * array [B + 1] with cu_seqlens[0] = 0, non-decreasing, cu_seqlens[B] = T;
+ * sequence b occupies tokens [cu_seqlens[b], cu_seqlens[b+1]); N is the
+ * maximum sequence length (it sizes the grid; a longer sequence is an
+ * error).  Query and key lengths are equal per sequence.
+ *
+ * Pointers: q..dv, lse, cu_seqlens, alibi_slopes and workspace are DEVICE
+ * pointers owned by the caller; the library allocates no device memory and
+ * keeps no per-call state.  bf16 tensors must start on a 16-byte boundary.
+ * `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
+ * asynchronous on `stream`; calls are not thread-safe on one stream.
+ *
+ * Errors.  Argument checks run on the host before any launch; a failing
+ * check returns its status and launches nothing.  Launch failures return
+ * FA_ERR_CUDA.  Faults found on the device (malformed cu_seqlens, a sequence
+ * longer than N, a pipeline wait that ran out of its time limit) set a
+ * per-device status word and make the affected blocks return early;
+ * fa_check_device_error() reads and clears it.  No C++ exception crosses
+ * this interface.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_NULL = 1,            /* a required pointer is NULL */
+  FA_ERR_SHAPE = 2,           /* negative / inconsistent sizes */
+  FA_ERR_UNSUPPORTED = 3,     /* valid but not implemented (d, dtype, scale) */
+  FA_ERR_ALIGN = 4,           /* a bf16 tensor not 16-byte aligned */
+  FA_ERR_WORKSPACE = 5,       /* workspace NULL or smaller than required */
+  FA_ERR_CUDA = 6,            /* a CUDA runtime / launch error */
+  FA_ERR_DEVICE_TIMEOUT = 7,  /* device: a pipeline wait exceeded its limit */
+  FA_ERR_CU_SEQLENS = 8       /* device: cu_seqlens malformed or length > N */
+} fa_status;
+
+typedef enum { FA_BF16 = 0, FA_FP32 = 1 } fa_dtype;
+
+/*
+ * Forward: writes o ([T, Hq, d], o_dtype) and lse ([Hq, T], float32).
+ *   B            number of sequences (>= 0)
+ *   Hq, Hkv      query / key-value heads, Hq % Hkv == 0 (GQA/MQA groups are
+ *                contiguous: kv head g serves query heads g*Hq/Hkv ...)
+ *   N            sequence length (dense) or maximum length (packed)
+ *   d            head dimension: bf16 d in {64, 128}; fp32 1 <= d <= 128
+ *   scale        softmax scale (> 0, finite), usually 1/sqrt(d)
+ *   causal       0 or 1
+ *   cu_seqlens   device int32 [B+1] or NULL (dense)
+ *   total_tokens T; for dense batches 0 or B*N
+ *   alibi_slopes device float32 [Hq] or NULL
+ *   dtype        element type of q, k, v
+ *   o_dtype      element type of o: FA_FP32 always allowed; FA_BF16 only
+ *                with dtype == FA_BF16.  bf16 storage alone rounds O by up
+ *                to 2^-9 |O| (1.6e-2 at |O| >= 4); FA_FP32 keeps the
+ *                kernel's fp32 result.
+ * FA_FP32 runs the fp32 SIMT kernel (forward only); FA_BF16 the tensor-core
+ * kernel (bf16 operands, fp32 accumulation and softmax).
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                 const int32_t* cu_seqlens, long long total_tokens,
+                 const float* alibi_slopes, fa_dtype dtype, fa_dtype o_dtype,
+                 void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: D (float32 [Hq, T]) and the dQ
+ * accumulator (float32 [Hq, T, d]), each 256-byte aligned.  T is
+ * total_tokens when > 0, else B*N.  Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, long long total_tokens);
+
+/*
+ * Backward: from q, k, v, the forward's o (element type o_dtype) and lse,
+ * and dO, writes dq ([T, Hq, d]), dk and dv ([T, Hkv, d]), all bf16.  Same
+ * size arguments as fa_fwd.  `workspace` (device, >= fa_bwd_workspace_size
+ * bytes, 256-byte aligned, contents irrelevant on entry) is scratch owned by
+ * the caller; it
+ * must not be used by anything else until the call completes on `stream`.
+ * dQ is accumulated with float32 reductions in an order that is not fixed,
+ * so dq may differ in the last bits from run to run.  Only FA_BF16.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
+                 const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                 int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                 const int32_t* cu_seqlens, long long total_tokens,
+                 const float* alibi_slopes, fa_dtype dtype, fa_dtype o_dtype,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * One stage of fa_bwd, with fa_bwd's arguments, so a caller can time or
+ * schedule the stages separately.  fa_bwd == the three stages in order on
+ * one stream:
+ *   FA_BWD_PREPROCESS  D = rowsum(dO o O) and the dQ accumulator zeroed
+ *                      (both in the workspace)
+ *   FA_BWD_DKDV        dk, dv, and dQ accumulated in the workspace
+ *   FA_BWD_DQ_CONVERT  dq = scale * accumulator, as bf16
+ * The same checks as fa_bwd run first; an unknown stage is
+ * FA_ERR_UNSUPPORTED.
+ */
+typedef enum { FA_BWD_PREPROCESS = 0, FA_BWD_DKDV = 1, FA_BWD_DQ_CONVERT = 2 } fa_bwd_stage_id;
+
+fa_status fa_bwd_stage(int stage, const void* q, const void* k, const void* v, const void* o,
+                       const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                       int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                       const int32_t* cu_seqlens, long long total_tokens,
+                       const float* alibi_slopes, fa_dtype dtype, fa_dtype o_dtype,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT, FA_ERR_CU_SEQLENS, or
+ * FA_ERR_CUDA if the synchronisation itself failed.
+ */
+fa_status fa_check_device_error(void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* fa_status_string(fa_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,109 @@
+"""The C ABI loads and validates its arguments on the host (CPU only).
+
+No test here launches a kernel: every call below is rejected (or is empty)
+before the library touches the GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_io_aware_36_gb300 import build, fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return fa.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    assert declared_functions() == sorted(fa.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        assert fa.fa_status_string(code)
+    assert "unknown" in fa.fa_status_string(99)
+    assert lib.fa_version() >= 10000
+
+
+A = 0x10000   # a fake, 256-byte aligned device address (never dereferenced)
+
+
+def fwd(**kw):
+    a = dict(q=A, k=A, v=A, o=A, lse=A, B=1, Hq=2, Hkv=2, N=128, d=64, scale=0.125, causal=1,
+             cu=None, T=0, alibi=None, dtype=fa.FA_BF16, odt=fa.FA_BF16, stream=None)
+    a.update(kw)
+    return fa.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["N"],
+                     a["d"], a["scale"], a["causal"], a["cu"], a["T"], a["alibi"], a["dtype"],
+                     a["odt"], a["stream"])
+
+
+def bwd(**kw):
+    a = dict(B=1, Hq=2, Hkv=2, N=128, d=64, scale=0.125, causal=1, cu=None, T=0, alibi=None,
+             dtype=fa.FA_BF16, odt=fa.FA_FP32, ws=A, wsb=1 << 40, stream=None, ptr=A)
+    a.update(kw)
+    p = a["ptr"]
+    return fa.fa_bwd(p, p, p, p, p, p, p, p, p, a["B"], a["Hq"], a["Hkv"], a["N"], a["d"],
+                     a["scale"], a["causal"], a["cu"], a["T"], a["alibi"], a["dtype"], a["odt"],
+                     a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(lse=None), 1), (dict(o=None), 1),
+    (dict(Hq=3, Hkv=2), 2), (dict(B=-1), 2), (dict(N=-5), 2), (dict(Hkv=0), 2),
+    (dict(T=999), 2),                      # dense batch with T != B*N
+    (dict(d=96), 3), (dict(d=256, dtype=fa.FA_FP32, odt=fa.FA_FP32), 3), (dict(dtype=7), 3),
+    (dict(scale=0.0), 3), (dict(scale=float("nan")), 3), (dict(scale=-1.0), 3),
+    (dict(q=A + 8), 4), (dict(v=A + 2), 4),
+    (dict(dtype=fa.FA_FP32, q=A + 2, odt=fa.FA_FP32), 4),
+    (dict(dtype=fa.FA_FP32, odt=fa.FA_BF16), 3), (dict(odt=5), 3),
+    (dict(B=0), 0), (dict(N=0), 0),        # empty: nothing to launch
+])
+def test_fwd_rejects_before_launch(lib, kw, code):
+    assert fwd(**kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ptr=None), 1), (dict(Hq=4, Hkv=3), 2), (dict(odt=9), 3), (dict(d=32), 3), (dict(dtype=fa.FA_FP32), 3),
+    (dict(ptr=A + 4), 4), (dict(ws=None), 5), (dict(wsb=1024), 5), (dict(ws=A + 16), 4),
+    (dict(B=0), 0),
+])
+def test_bwd_rejects_before_launch(lib, kw, code):
+    assert bwd(**kw) == code
+
+
+def test_bwd_stage_rejects_unknown_stage(lib):
+    p = A
+    args = (p, p, p, p, p, p, p, p, p, 1, 2, 2, 128, 64, 0.125, 1, None, 0, None, fa.FA_BF16,
+            fa.FA_FP32, A, 1 << 40, None)
+    assert fa.fa_bwd_stage(3, *args) == 3
+    assert fa.fa_bwd_stage(-1, *args) == 3
+    bad = list(args)
+    bad[0] = None
+    assert fa.fa_bwd_stage(0, *bad) == 1
+
+
+def test_workspace_size(lib):
+    T, Hq, d = 1000, 3, 64
+    n = fa.fa_bwd_workspace_size(1, Hq, T, d, 0)
+    r = lambda x: (x + 255) // 256 * 256
+    assert n == r(Hq * T * 4) + r(Hq * T * d * 4)
+    assert fa.fa_bwd_workspace_size(2, Hq, 4096, d, T) == n   # packed: T given
+    assert fa.fa_bwd_workspace_size(-1, Hq, T, d, 0) == 0
