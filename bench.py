@@ -1,0 +1,415 @@
+#!/usr/bin/env python
+"""Benchmark: causal bf16 attention forward + backward TFLOP/s on one GB300.
+
+One step is one pass of the whole hot path over one batch: the forward
+kernel (O, LSE), then the three backward kernels (D and dQ-accumulator
+reset; dK, dV and dQ accumulation; dQ convert).  The default workload is the
+long-context configuration B=1, H=32, N=16384, d=128, causal, bf16 (q, k
+scaled by 0.5), the one the throughput target is stated on.  Inputs are
+seeded synthetic data (no dataset), resident in HBM before the timed region;
+they total 537 MB, larger than the 126 MB L2, so no flush is needed between
+steps.
+
+FLOPs are algorithmic: 4*d per attended pair forward, 10*d backward (five
+MMAs, with the recomputation of S counted), so 14*d*pairs per step; causal
+pairs are L(L+1)/2 per sequence and head.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun each rank runs its own replica (the path shards into
+independent problems; there is no data-path collective): "scaling": "weak".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from exact_io_aware_36_gb300 import inputs as I  # noqa: E402
+
+METRIC = "causal bf16 attention fwd+bwd TFLOP/s on 1 GB300; % of dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_dram_traffic.json")
+FALLBACK_BF16_TFLOPS = 1900.0
+KERNEL_SOURCES = {"fwd": "fa_fwd_bf16.cu", "bwd_dkdv": "fa_bwd_bf16.cu",
+                  "bwd_preprocess": "fa_bwd_bf16.cu", "bwd_dq_convert": "fa_bwd_bf16.cu"}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="c3_long", choices=sorted(I.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def flops_per_step(w: I.Workload, seqlens) -> dict:
+    pairs = I.attended_pairs(w, seqlens)
+    return {"pairs": pairs, "fwd": 4.0 * w.d * pairs, "bwd": 10.0 * w.d * pairs,
+            "total": (14.0 if w.backward else 4.0) * w.d * pairs}
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), float(pk.get("hbm_gbs", 0.0)), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, 6800.0, "fallback"
+
+
+def source_hash(name: str) -> str:
+    src = os.path.join(ROOT, "exact_io_aware_36_gb300", "csrc", name)
+    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if
+    the kernel's source is unchanged since the counters were taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)[kernel]
+        if source_hash(rec["source"]) != rec["source_sha256_16"]:
+            return None
+        return rec["bytes_per_launch"]
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        reasons = sorted({self.NAMES[i] for *_, fl in rows for i, v in enumerate(fl)
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+def smi_index(local: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    parts = [p for p in vis.split(",") if p.strip()]
+    if local < len(parts) and parts[local].strip().isdigit():
+        return int(parts[local])
+    return local
+
+
+# --------------------------------------------------------------------- ours
+
+def run_ours(args, world, rank, local):
+    import torch
+    from exact_io_aware_36_gb300 import fa
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = I.workload(args.workload)
+    x = I.make_inputs(w, seed=0)
+    fl = flops_per_step(w, x.seqlens)
+    T = x.T
+
+    def todev(name):
+        return torch.from_numpy(x.bits[name].view("int16")).view(torch.bfloat16).to(dev)
+
+    q, k, v = todev("q"), todev("k"), todev("v")
+    do = todev("do") if w.backward else None
+    o = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    lse = torch.empty((w.Hq, T), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    cu = torch.from_numpy(x.cu_seqlens).to(dev) if w.varlen else None
+    slopes = torch.from_numpy(x.alibi_slopes).to(dev) if w.alibi else None
+    ws_bytes = fa.fa_bwd_workspace_size(w.B, w.Hq, w.N, w.d, T)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    P = lambda t: None if t is None else t.data_ptr()
+    common = (w.B, w.Hq, w.Hkv, w.N, w.d, float(x.scale), int(w.causal), P(cu), T, P(slopes))
+    ptrs = (P(q), P(k), P(v), P(o), P(do), P(lse), P(dq), P(dk), P(dv))
+    names = ["fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq_convert"]
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        st = fa.fa_fwd(ptrs[0], ptrs[1], ptrs[2], ptrs[3], ptrs[5], *common, fa.FA_BF16,
+                       fa.FA_FP32, sp)
+        if st:
+            raise fa.FAError(st, "fa_fwd")
+        if not w.backward:
+            if evs is not None:
+                evs[1].record(stream)
+            return
+        for s in range(3):
+            if evs is not None:
+                evs[1 + s].record(stream)
+            st = fa.fa_bwd_stage(s, *ptrs, *common, fa.FA_BF16, fa.FA_FP32, P(ws), ws_bytes, sp)
+            if st:
+                raise fa.FAError(st, "fa_bwd_stage")
+        if evs is not None:
+            evs[4].record(stream)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize(dev)
+    st = fa.fa_check_device_error(sp)
+    if st:
+        raise fa.FAError(st, "warm-up")
+
+    nev = 5 if w.backward else 2
+    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(smi_index(local))
+    sampler.start()
+    time.sleep(0.1)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        step(evsets[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    st = fa.fa_check_device_error(sp)
+    if st:
+        raise fa.FAError(st, "timed region")
+    total_ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    value = world * fl["total"] / (ms_step * 1e-3) / 1e12
+
+    kern_ms = {}
+    for j, name in enumerate(names[:nev - 1]):
+        kern_ms[name] = statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evsets)
+    kern_flops = {"fwd": fl["fwd"], "bwd_dkdv": fl["bwd"]}
+    dom = max(kern_ms, key=lambda n: kern_ms[n])
+    peak, hbm, peak_src = load_peaks()
+    if dom in kern_flops:
+        ach = kern_flops[dom] / (kern_ms[dom] * 1e-3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+                "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
+                "traffic": ncu_traffic(dom)}
+    else:
+        roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s",
+                "frac": None, "traffic": ncu_traffic(dom)}
+    per_kernel = {n: {"ms": round(kern_ms[n], 4),
+                      "tflops": round(kern_flops[n] / (kern_ms[n] * 1e-3) / 1e12, 1)
+                      if n in kern_flops else None,
+                      "share": round(kern_ms[n] / sum(kern_ms.values()), 4)}
+                  for n in kern_ms}
+    fwd_tflops = fl["fwd"] / (kern_ms["fwd"] * 1e-3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, x, fl, world, dev, stream, step,
+                      [(q, "q"), (k, "k"), (v, "v")] + ([(do, "do")] if w.backward else []),
+                      [o, lse] + ([dq, dk, dv] if w.backward else []))
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, x)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded PCG64, seed 0; no dataset)",
+        "config": {"workload": w.name, "desc": w.note, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "N": w.N, "d": w.d, "causal": w.causal, "alibi": w.alibi, "varlen": w.varlen,
+                   "total_tokens": T, "o_dtype": "fp32", "flops_per_step": fl["total"],
+                   "pct_of_peak": round(100.0 * value / world / peak, 2),
+                   "fwd_tflops": round(fwd_tflops, 1),
+                   "fwd_pct_of_peak": round(100.0 * fwd_tflops / peak, 2),
+                   "l2": "inputs exceed L2 (537 MB at c3_long); no flush between steps",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "per_kernel": per_kernel,
+        "roofline": roof,
+        "gpu_launches": args.steps * (4 if w.backward else 1),
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, w, x, fl, world, dev, stream, step, ins, outs):
+    """Same metric through the C ABI with host buffers: every step copies its
+    inputs from pinned host memory and its outputs back, inside the timing."""
+    import torch
+    hins = [(d, torch.from_numpy(x.bits[n].view("int16")).view(torch.bfloat16).pin_memory())
+            for d, n in ins]
+    houts = [(d, torch.empty(d.shape, dtype=d.dtype, pin_memory=True)) for d in outs]
+    h2d = sum(h.numel() * h.element_size() for _, h in hins)
+    d2h = sum(h.numel() * h.element_size() for _, h in houts)
+
+    def e2e_step():
+        for d, h in hins:
+            d.copy_(h, non_blocking=True)
+        step()
+        for d, h in houts:
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    n = max(3, args.steps // 3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / n
+    return {"value": round(world * fl["total"] / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
+            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "path": "fa_fwd + fa_bwd_stage x3 through the C ABI, pinned host buffers"}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_sample(w: I.Workload, x):
+    """One whole (sequence, query head) of the workload, forward + backward
+    in fp64, with the oracle as it stands."""
+    from oracle import attention_fp64 as A
+    s, e = int(x.cu_seqlens[0]), int(x.cu_seqlens[1])
+    h, g = 0, 0
+    slope = None if x.alibi_slopes is None else float(x.alibi_slopes[h])
+    L = e - s
+    pairs = L * (L + 1) // 2 if w.causal else L * L
+    t0 = time.perf_counter()
+    if w.backward:
+        A.head_backward(x.q[s:e, h], x.k[s:e, g], x.v[s:e, g], x.do[s:e, h], x.scale, w.causal,
+                        slope)
+    else:
+        A.head_forward(x.q[s:e, h], x.k[s:e, g], x.v[s:e, g], x.scale, w.causal, slope)
+    dt = time.perf_counter() - t0
+    flops = (14.0 if w.backward else 4.0) * w.d * pairs
+    return flops, dt, f"1 of {w.B * w.Hq} (sequence, query head) pairs: sequence 0 (L={L}), head 0"
+
+
+def cpu_baseline(w, x):
+    fl, dt, sample = oracle_sample(w, x)
+    return {"value": round(fl / dt / 1e12, 6), "unit": UNIT, "cores": os.cpu_count(),
+            "kind": "oracle", "sample": sample, "seconds": round(dt, 2),
+            "note": "NumPy float64, materialises S and P; BLAS threads = all cores"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = I.workload(args.workload)
+    x = I.make_inputs(w, seed=0)
+    for _ in range(max(args.warmup, 0)):
+        oracle_sample(w, x)
+    tot_fl, tot_dt, sample = 0.0, 0.0, ""
+    for _ in range(args.steps):
+        fl, dt, sample = oracle_sample(w, x)
+        tot_fl += fl
+        tot_dt += dt
+    value = tot_fl / tot_dt / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot_dt / max(args.steps, 1), 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded PCG64, seed 0; no dataset)", "impl": "reference",
+        "config": {"workload": w.name, "desc": w.note, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "N": w.N, "d": w.d, "causal": w.causal,
+                   "step": "one (sequence, head) sample of the workload per step"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_info()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    try:
+        run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
