@@ -25,7 +25,7 @@ STATUS = {
     5: "FA_ERR_WORKSPACE", 6: "FA_ERR_CUDA", 7: "FA_ERR_DEVICE_TIMEOUT", 8: "FA_ERR_CU_SEQLENS",
 }
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_stage", "fa_bwd_workspace_size", "fa_check_device_error",
-           "fa_status_string", "fa_version")
+           "fa_status_string", "fa_version", "fa_bwd_static_scratch")
 FA_BWD_PREPROCESS, FA_BWD_DKDV, FA_BWD_DQ_CONVERT = 0, 1, 2
 
 
@@ -95,6 +95,23 @@ def fa_bwd_stage(stage, q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale
     return load().fa_bwd_stage(stage, q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale,
                                int(causal), cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype,
                                workspace, workspace_bytes, stream)
+
+
+FA_BWD_STATIC_SCRATCH_BYTES = 64 << 20
+
+
+def fa_bwd_static_scratch(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal,
+                          cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype, stream) -> int:
+    """fa_bwd without a workspace argument, for callers that cannot allocate
+    device memory: the scratch lives in a fixed array of
+    FA_BWD_STATIC_SCRATCH_BYTES inside the library (see include/fa.h)."""
+    lib = load()
+    fn = lib.fa_bwd_static_scratch
+    if fn.restype is not ctypes.c_int or not fn.argtypes:
+        fn.argtypes = lib.fa_bwd.argtypes[:21] + [ctypes.c_void_p]
+        fn.restype = ctypes.c_int
+    return fn(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, int(causal), cu_seqlens,
+              total_tokens, alibi_slopes, dtype, o_dtype, stream)
 
 
 def fa_bwd_workspace_size(B, Hq, N, d, total_tokens) -> int:

@@ -141,6 +141,46 @@ fa_status fa_bwd_stage(int stage, const void* q, const void* k, const void* v, c
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fa_bwd for callers that cannot allocate device memory.  (The pages have no
+ * counterpart: this is an interface convenience of this library.)
+ *
+ * Some callers cannot hand fa_bwd a workspace: a plugin or custom-op hook
+ * in another framework that gets no workspace and cannot reach that
+ * framework's allocator, a runtime that fixes its device memory at start-up
+ * and allows no allocation later, or code that must not call cudaMalloc
+ * because it would synchronise the device or disturb a stream capture.
+ * This entry point takes the same arguments as fa_bwd minus the workspace,
+ * runs the same kernels, and keeps D and the dQ accumulator in a fixed
+ * array of FA_BWD_STATIC_SCRATCH_BYTES inside the library's device memory.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * - Limit: a problem needing more than FA_BWD_STATIC_SCRATCH_BYTES of
+ *   workspace (fa_bwd_workspace_size) is refused with FA_ERR_WORKSPACE
+ *   before anything is launched.  64 MiB holds about 130,000 (token,
+ *   query head) rows at d = 128 and 258,000 at d = 64, e.g. B = 8, H = 16,
+ *   N = 1024, d = 64 (34 MB).
+ * - Memory: every GPU that loads the library holds the array until the
+ *   process exits, whether or not this entry point is used.
+ * - Set-up: the first call with a given device current looks up the
+ *   array's device address (cudaGetSymbolAddress) and caches it; make that
+ *   first call before any stream capture on that device.
+ * - Sharing: all calls on a device use the same array and it keeps the last
+ *   call's contents.  Each call rewrites everything it reads (D, and a
+ *   zeroed dQ accumulator), but calls that overlap on the GPU (different
+ *   streams, or host threads, without ordering between them) race on it:
+ *   order them on one stream or synchronise between them.
+ * - Other errors: as fa_bwd.
+ */
+#define FA_BWD_STATIC_SCRATCH_BYTES (64ull << 20)
+
+fa_status fa_bwd_static_scratch(const void* q, const void* k, const void* v, const void* o,
+                                const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                                int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                                const int32_t* cu_seqlens, long long total_tokens,
+                                const float* alibi_slopes, fa_dtype dtype, fa_dtype o_dtype,
+                                void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status
  * word.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT, FA_ERR_CU_SEQLENS, or
  * FA_ERR_CUDA if the synchronisation itself failed.

@@ -1,0 +1,83 @@
+"""fa_bwd_static_scratch: the backward for callers that cannot allocate.
+
+Plugins or custom-op hooks that get no workspace, runtimes that forbid
+device allocation after start-up, and code that must not call cudaMalloc on
+its hot path use this entry point instead of fa_bwd; it keeps its scratch in
+a fixed array inside the library.  These tests call it through the C ABI and
+compare it with fa_bwd (given a workspace allocated here) on two calls in a
+row, with different problem sizes, so the second call runs over whatever the
+first left in the shared array.  Same tolerance as the other backward parity
+tests: 2e-2 x max |grad| per gradient tensor.
+
+This file is named to be collected last, so a run that stops at the first
+failure has run every other test before it.
+"""
+import numpy as np
+import pytest
+
+from exact_io_aware_36_gb300 import build, fa
+from exact_io_aware_36_gb300 import inputs as I
+
+TOL_GRAD = 2e-2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return fa.load()
+
+
+def test_refuses_problems_larger_than_the_scratch(lib):
+    """A problem whose workspace exceeds the fixed array is refused with
+    FA_ERR_WORKSPACE before any CUDA call (runs without a GPU)."""
+    A = 0x10000
+    B, Hq, N, d = 1, 32, 16384, 128
+    assert fa.fa_bwd_workspace_size(B, Hq, N, d, 0) > fa.FA_BWD_STATIC_SCRATCH_BYTES
+    st = fa.fa_bwd_static_scratch(A, A, A, A, A, A, A, A, A, B, Hq, Hq, N, d, 0.088, 1, None, 0,
+                                  None, fa.FA_BF16, fa.FA_FP32, None)
+    assert st == 5
+
+
+def _run_pair(w, seed):
+    """fa_fwd, then fa_bwd (caller workspace) and fa_bwd_static_scratch on the
+    same inputs; returns both gradient triples as float64 arrays."""
+    import torch
+    x = I.make_inputs(w, seed=seed)
+    dev = lambda n: torch.from_numpy(x.bits[n].view(np.int16)).view(torch.bfloat16).cuda()
+    q, k, v, do = dev("q"), dev("k"), dev("v"), dev("do")
+    cu = torch.from_numpy(x.cu_seqlens).cuda() if w.varlen else None
+    slopes = torch.from_numpy(x.alibi_slopes).cuda() if w.alibi else None
+    T = x.T
+    o = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    lse = torch.empty((w.Hq, T), dtype=torch.float32, device="cuda")
+    sp = torch.cuda.current_stream().cuda_stream
+    P = lambda t: None if t is None else t.data_ptr()
+    common = (w.B, w.Hq, w.Hkv, w.N, w.d, float(x.scale), int(w.causal), P(cu), T, P(slopes))
+    assert fa.fa_fwd(P(q), P(k), P(v), P(o), P(lse), *common, fa.FA_BF16, fa.FA_FP32, sp) == 0
+    ref = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
+    ws_bytes = fa.fa_bwd_workspace_size(w.B, w.Hq, w.N, w.d, T)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    assert fa.fa_bwd(P(q), P(k), P(v), P(o), P(do), P(lse), *(P(t) for t in ref), *common,
+                     fa.FA_BF16, fa.FA_FP32, P(ws), ws_bytes, sp) == 0
+    got = [torch.full_like(q, float("nan")), torch.full_like(k, float("nan")),
+           torch.full_like(v, float("nan"))]
+    assert fa.fa_bwd_static_scratch(P(q), P(k), P(v), P(o), P(do), P(lse), *(P(t) for t in got),
+                                    *common, fa.FA_BF16, fa.FA_FP32, sp) == 0
+    assert fa.fa_check_device_error(sp) == 0
+    f64 = lambda t: t.double().cpu().numpy()
+    return [f64(t) for t in ref], [f64(t) for t in got]
+
+
+@pytest.mark.gpu
+def test_matches_fa_bwd_on_two_calls_in_a_row(lib):
+    cases = [
+        # larger first, so the second call reuses a scratch holding stale data
+        I.small_case("bf16", causal=True, B=2, Hq=4, Hkv=2, N=520, d=128, alibi=True),
+        I.small_case("bf16", causal=True, Hq=2, Hkv=1, d=64, seqlens=(17, 300, 1)),
+    ]
+    for n, w in enumerate(cases):
+        ref, got = _run_pair(w, seed=40 + n)
+        for name, r, g in zip(("dQ", "dK", "dV"), ref, got):
+            assert np.isfinite(g).all(), (n, name)
+            err = np.abs(g - r).max() / max(np.abs(r).max(), 1e-30)
+            assert err <= TOL_GRAD, (n, name, err)
