@@ -82,11 +82,16 @@ struct BwdBars {
 };
 static_assert(sizeof(BwdBars) <= 128, "barrier block");
 
-struct Side {
-  float L2[64];
+// Per-step query statistics, written by the producer warp:
+//   nL2[q] = -LSE_q * log2(e) - slope2 * q   (-inf for queries past the
+//            sequence end, so their P is exactly 0; slope2 = 0 without ALiBi)
+//   Dv[q]  = D_q                              (0 past the end)
+struct alignas(16) Side {
+  float nL2[64];
   float Dv[64];
   float slope2;
 };
+static_assert(sizeof(Side) == 528, "side buffer stride");
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -261,7 +266,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const int qq = lane + 32 * r;
         const bool valid = q0 + qq < L;
         const long long idx = (long long)h * p.T + seq0 + q0 + qq;
-        sd->L2[qq] = valid ? __ldg(p.lse + idx) * kLog2e : INFINITY;
+        const float sl2 = ALIBI ? __ldg(p.alibi + h) * kLog2e : 0.f;
+        sd->nL2[qq] = valid ? fmaf(-sl2, (float)qq, -__ldg(p.lse + idx) * kLog2e) : -INFINITY;
         sd->Dv[qq] = valid ? __ldg(p.D + idx) : 0.f;
       }
       if (lane == 0) sd->slope2 = ALIBI ? __ldg(p.alibi + h) * kLog2e : 0.f;
@@ -380,8 +386,12 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tc_fence_after();
       const Side* sd = side + st;
       const bool need_mask = (CAUSAL && q0 < n0 + 127) || !key_ok;
-      const float slope2 = ALIBI ? sd->slope2 : 0.f;
-      const float bias0 = ALIBI ? slope2 * (float)(key - q0) : 0.f;
+      // x = S^T * scale * log2(e) + slope2 * (key - q0) + nL2[q]: the bias
+      // term is split into a per-thread part (key - q0, exact integer) and a
+      // per-query part folded into nL2 by the producer.
+      const float kb = ALIBI ? sd->slope2 * (float)(key - q0) : 0.f;
+      const uint64_t c2p = f2(c2, c2);
+      const uint64_t kbp = f2(kb, kb);
       uint8_t* dsrow = smem + C::DS_OFF + buf * C::DS_BYTES + kr * 128;
       const uint32_t tSb = lane_base + C::SB_COL0 + 64 * buf;
       const uint32_t tPb = lane_base + C::PB_COL0 + 64 * buf;
@@ -394,22 +404,33 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         reg_fence32(sv);
         reg_fence32(dp);
         uint32_t pk[16], dk[16];
+        const float4* nl4 = reinterpret_cast<const float4*>(sd->nL2 + 32 * half);
+        const float4* dd4 = reinterpret_cast<const float4*>(sd->Dv + 32 * half);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          float pv[2], dv2[2];
+        for (int g4 = 0; g4 < 8; ++g4) {        // 4 queries per group
+          const float4 nl = nl4[g4];
+          const float4 dd = dd4[g4];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int ql = 2 * c + e;            // query within the half
-            const int qq = 32 * half + ql;       // query within the tile
-            float x = __uint_as_float(sv[ql]) * c2;
-            if (ALIBI) x = fmaf(-slope2, (float)qq, x + bias0);
-            float pr = ex2_approx(x - sd->L2[qq]);
-            if (need_mask && (!key_ok || (CAUSAL && key > q0 + qq))) pr = 0.f;
-            pv[e] = pr;
-            dv2[e] = pr * (__uint_as_float(dp[ql]) - sd->Dv[qq]);
+          for (int pr = 0; pr < 2; ++pr) {
+            const int ql = 4 * g4 + 2 * pr;     // query within the half
+            uint64_t bias = pr ? f2(nl.z, nl.w) : f2(nl.x, nl.y);
+            if (ALIBI) bias = fadd2(bias, kbp);
+            float x0, x1;
+            f2split(ffma2(f2(__uint_as_float(sv[ql]), __uint_as_float(sv[ql + 1])), c2p, bias), x0, x1);
+            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            if (need_mask) {
+              const int q = q0 + 32 * half + ql;
+              if (!key_ok || (CAUSAL && key > q)) p0 = 0.f;
+              if (!key_ok || (CAUSAL && key > q + 1)) p1 = 0.f;
+            }
+            const uint64_t pp = f2(p0, p1);
+            const uint64_t dsd = fmul2(pp, fsub2(f2(__uint_as_float(dp[ql]), __uint_as_float(dp[ql + 1])),
+                                                 pr ? f2(dd.z, dd.w) : f2(dd.x, dd.y)));
+            float d0, d1;
+            f2split(dsd, d0, d1);
+            pk[ql / 2] = pack_bf16x2(p0, p1);
+            dk[ql / 2] = pack_bf16x2(d0, d1);
           }
-          pk[c] = pack_bf16x2(pv[0], pv[1]);
-          dk[c] = pack_bf16x2(dv2[0], dv2[1]);
         }
         tmem_st16(tSb + 16 * half, pk);          // P^T (bf16) over consumed S^T columns
         tmem_st16(tPb + 16 * half, dk);          // dS^T (bf16) over consumed dP^T columns

@@ -271,7 +271,11 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       reg_fence32(s + 96);
       const int n0 = 128 * j;
       const bool need_mask = (CAUSAL && n0 + 127 > m0 + 128 * t) || (n0 + 128 > L);
-      float xmax = -INFINITY;
+      // Row max over four independent chains of 3-input max (short
+      // dependency chains: one softmax warp per SM sub-partition at a time).
+      float mx[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
       if (ALIBI) {
         const float base = slope2 * (float)(n0 - row);
 #pragma unroll
@@ -282,20 +286,21 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             if (key >= L || (CAUSAL && key > row)) x = -INFINITY;
           }
           s[c] = __float_as_uint(x);
-          xmax = fmaxf(xmax, x);
         }
-      } else {
-        if (need_mask) {
+      } else if (need_mask) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            const int key = n0 + c;
-            if (key >= L || (CAUSAL && key > row)) s[c] = __float_as_uint(-INFINITY);
-          }
+        for (int c = 0; c < 128; ++c) {
+          const int key = n0 + c;
+          if (key >= L || (CAUSAL && key > row)) s[c] = __float_as_uint(-INFINITY);
         }
-#pragma unroll
-        for (int c = 0; c < 128; ++c) xmax = fmaxf(xmax, __uint_as_float(s[c]));
-        xmax *= c2;
       }
+#pragma unroll
+      for (int c = 0; c < 128; c += 8)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          mx[i] = fmax3(mx[i], __uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1]));
+      float xmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
+      if (!ALIBI) xmax *= c2;
       // lazy rescale: raise the reference only when the max grew past tau
       const bool raise = xmax > m_ref + kTau;
       const float m_new = raise ? xmax : m_ref;
@@ -316,25 +321,36 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
       m_ref = m_new;
       const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
-      float rs = 0.f, rsr = 0.f;
-      // P in chunks of 32 scores -> 16 packed columns, stored as produced
+      // p = 2^(x - m): packed f32x2 scale-and-subtract, MUFU exp2, and two
+      // sums (exact p; bf16-rounded p) in two independent packed chains each.
+      const uint64_t c2p = f2(c2, c2);
+      const uint64_t nmb = f2(-mb, -mb);
+      uint64_t acc[2] = {0, 0}, accr[2] = {0, 0};
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const float x0 = __uint_as_float(s[32 * ch + 2 * c]);
-          const float x1 = __uint_as_float(s[32 * ch + 2 * c + 1]);
-          const float p0 = ALIBI ? ex2_approx(x0 - mb) : ex2_approx(fmaf(x0, c2, -mb));
-          const float p1 = ALIBI ? ex2_approx(x1 - mb) : ex2_approx(fmaf(x1, c2, -mb));
-          rs += p0 + p1;
+          const uint64_t xy = f2(__uint_as_float(s[32 * ch + 2 * c]), __uint_as_float(s[32 * ch + 2 * c + 1]));
+          const uint64_t e = ALIBI ? fadd2(xy, nmb) : ffma2(xy, c2p, nmb);
+          float e0, e1;
+          f2split(e, e0, e1);
+          const float p0 = ex2_approx(e0);
+          const float p1 = ex2_approx(e1);
+          acc[c & 1] = fadd2(acc[c & 1], f2(p0, p1));
           pk[c] = pack_bf16x2(p0, p1);
-          rsr += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xFFFF0000u);
+          accr[c & 1] = fadd2(accr[c & 1], f2(__uint_as_float(pk[c] << 16),
+                                               __uint_as_float(pk[c] & 0xFFFF0000u)));
         }
         tmem_st16(tS + 16 * ch, pk);
       }
-      l += rs;
-      lr += rsr;
+      {
+        float a0, a1, b0, b1;
+        f2split(fadd2(acc[0], acc[1]), a0, a1);
+        f2split(fadd2(accr[0], accr[1]), b0, b1);
+        l += a0 + a1;
+        lr += b0 + b1;
+      }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();

@@ -39,6 +39,49 @@ __device__ __forceinline__ float lg2_approx(float x) {
   return y;
 }
 
+// max of three floats in one instruction (sm_100 family).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Packed pairs of fp32 (one 64-bit register pair) and the sm_100-family
+// f32x2 arithmetic on them: one instruction issues two lanes' worth of work.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void f2split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t fsub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // Two fp32 -> packed bf16x2 (round to nearest even); `lo` in bits 0..15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
@@ -85,25 +128,32 @@ struct WaitCtx {
   unsigned int* status;       // global per-device status word
 };
 
-// Warp-collective bounded wait for the phase of `bar` with parity `parity`.
-// All 32 lanes must call it; the result is warp-uniform.
-__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
-  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-  uint64_t t0 = globaltimer_ns();
+// Slow path of wait_warp, kept out of line so the timer state does not add
+// register pressure to the loops that wait.
+static __device__ __noinline__ bool wait_warp_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                            unsigned int* status) {
+  const uint64_t t0 = globaltimer_ns();
   while (true) {
     bool ok = mbar_try_wait(bar, parity);
     if (__all_sync(0xffffffffu, ok)) return true;
     int bad = 0;
     if ((threadIdx.x & 31) == 0) {
-      if (*w.abort_flag) bad = 1;
+      if (*abort_flag) bad = 1;
       else if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        *w.abort_flag = 1;
-        record_status(w.status, FA_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
+        record_status(status, FA_ERR_DEVICE_TIMEOUT);
         bad = 1;
       }
     }
     if (__shfl_sync(0xffffffffu, bad, 0)) return false;
   }
+}
+
+// Warp-collective bounded wait for the phase of `bar` with parity `parity`.
+// All 32 lanes must call it; the result is warp-uniform.
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  return wait_warp_slow(bar, parity, w.abort_flag, w.status);
 }
 
 // Bounded wait that ignores the abort flag, used while unwinding: copies and
