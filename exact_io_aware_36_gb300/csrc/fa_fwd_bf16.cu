@@ -7,8 +7,11 @@
 // row), Key design 4 (FA3-style asynchrony: producer and consumer roles).
 //
 // GB300 mapping (one CTA per SM, 320 threads, 2 query tiles of 128 rows):
-//   warp 9     TMA producer: Q0/Q1 once, then K_j and V_j into a ring of
-//              STAGES slots (128-byte swizzle), mbarrier full/empty pairs.
+//   warp 9     TMA producer: Q0/Q1 once, then K_j and V_j into two rings
+//              (128-byte swizzle) with their own full/empty mbarriers: a K
+//              slot is released once both S MMAs of its tile are done, a V
+//              slot once both PV MMAs are, so the next K load never waits
+//              for the slower V release.
 //   warp 8     MMA issuer (one lane): S_t = Q_t K_j^T into TMEM (both
 //              operands K-major in shared memory), then O_t += P_t V_j with
 //              P_t read from TMEM and V_j MN-major in shared memory.
@@ -45,11 +48,12 @@ struct FwdCfg {
   static constexpr int NB = D / 64;                 // 64-column boxes per row
   static constexpr int BOX_BYTES = 128 * 64 * 2;    // one 128 x 64 bf16 box
   static constexpr int TILE_BYTES = NB * BOX_BYTES; // one 128 x D tile
-  static constexpr int STAGES = D == 128 ? 2 : 4;
+  static constexpr int KS = D == 128 ? 3 : 6;      // K ring stages
+  static constexpr int VS = D == 128 ? 2 : 4;      // V ring stages
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + 2 * TILE_BYTES;
-  static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
-  static constexpr int BAR_OFF = V_OFF + STAGES * TILE_BYTES;
+  static constexpr int V_OFF = K_OFF + KS * TILE_BYTES;
+  static constexpr int BAR_OFF = V_OFF + VS * TILE_BYTES;
   static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
   static constexpr uint32_t S_COL0 = 0, S_COL1 = 128;
   static constexpr uint32_t O_COL0 = 256, O_COL1 = 256 + D;
@@ -57,7 +61,7 @@ struct FwdCfg {
 
 struct FwdBars {
   uint64_t q_full;
-  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t k_full[8], k_empty[8], v_full[8], v_empty[8];
   uint64_t s_full[2], p_full[2];
   uint64_t o_done;
   uint32_t tmem_base;
@@ -113,7 +117,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
+    for (int s = 0; s < 8; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
       mbar_init(&bars->v_full[s], 1);
@@ -153,35 +157,37 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                       (int)(seq0 + m0 + 128 * t), &bars->q_full);
     }
     __syncwarp();
-    int issued = 0;                 // K/V tiles whose loads were issued
+    int issued_k = 0, issued_v = 0;   // tiles whose loads were issued
     for (int j = 0; j < nkv_max; ++j) {
-      const int s = j % C::STAGES;
-      const uint32_t ph = ((j / C::STAGES) & 1) ^ 1;
-      if (!wait_warp(&bars->k_empty[s], ph, wc)) break;
-      if (!wait_warp(&bars->v_empty[s], ph, wc)) break;
+      const int sk = j % C::KS;
+      if (!wait_warp(&bars->k_empty[sk], ((j / C::KS) & 1) ^ 1, wc)) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->k_full[s], C::TILE_BYTES);
+        mbar_arrive_expect_tx(&bars->k_full[sk], C::TILE_BYTES);
 #pragma unroll
         for (int bx = 0; bx < C::NB; ++bx)
-          tma_load_3d(smem + C::K_OFF + s * C::TILE_BYTES + bx * C::BOX_BYTES, &tmK, bx * 64, kvh,
-                      (int)(seq0 + 128 * j), &bars->k_full[s]);
-        mbar_arrive_expect_tx(&bars->v_full[s], C::TILE_BYTES);
-#pragma unroll
-        for (int bx = 0; bx < C::NB; ++bx)
-          tma_load_3d(smem + C::V_OFF + s * C::TILE_BYTES + bx * C::BOX_BYTES, &tmV, bx * 64, kvh,
-                      (int)(seq0 + 128 * j), &bars->v_full[s]);
+          tma_load_3d(smem + C::K_OFF + sk * C::TILE_BYTES + bx * C::BOX_BYTES, &tmK, bx * 64, kvh,
+                      (int)(seq0 + 128 * j), &bars->k_full[sk]);
       }
       __syncwarp();
-      issued = j + 1;
+      issued_k = j + 1;
+      const int sv = j % C::VS;
+      if (!wait_warp(&bars->v_empty[sv], ((j / C::VS) & 1) ^ 1, wc)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->v_full[sv], C::TILE_BYTES);
+#pragma unroll
+        for (int bx = 0; bx < C::NB; ++bx)
+          tma_load_3d(smem + C::V_OFF + sv * C::TILE_BYTES + bx * C::BOX_BYTES, &tmV, bx * 64, kvh,
+                      (int)(seq0 + 128 * j), &bars->v_full[sv]);
+      }
+      __syncwarp();
+      issued_v = j + 1;
     }
     // Loads in flight must land before this CTA's shared memory goes away.
     wait_warp_drain(&bars->q_full, 0);
-    for (int j = max(0, issued - C::STAGES); j < issued; ++j) {
-      const int s = j % C::STAGES;
-      const uint32_t ph = (j / C::STAGES) & 1;
-      wait_warp_drain(&bars->k_full[s], ph);
-      wait_warp_drain(&bars->v_full[s], ph);
-    }
+    for (int j = max(0, issued_k - C::KS); j < issued_k; ++j)
+      wait_warp_drain(&bars->k_full[j % C::KS], (j / C::KS) & 1);
+    for (int j = max(0, issued_v - C::VS); j < issued_v; ++j)
+      wait_warp_drain(&bars->v_full[j % C::VS], (j / C::VS) & 1);
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);
@@ -193,10 +199,10 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const uint32_t colO[2] = {C::O_COL0, C::O_COL1};
     bool ok = wait_warp(&bars->q_full, 0, wc);
     for (int j = 0; ok && j <= nkv_max; ++j) {
-      const int sj = j % C::STAGES;
-      const int sp = (j + C::STAGES - 1) % C::STAGES;
-      if (j < nkv_max && !(ok = wait_warp(&bars->k_full[sj], (j / C::STAGES) & 1, wc))) break;
-      if (j >= 1 && !(ok = wait_warp(&bars->v_full[sp], ((j - 1) / C::STAGES) & 1, wc))) break;
+      const int sj = j % C::KS;                       // K_j
+      const int sp = (j + C::VS - 1) % C::VS;         // V_{j-1}
+      if (j < nkv_max && !(ok = wait_warp(&bars->k_full[sj], (j / C::KS) & 1, wc))) break;
+      if (j >= 1 && !(ok = wait_warp(&bars->v_full[sp], ((j - 1) / C::VS) & 1, wc))) break;
       tc_fence_after();
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
