@@ -14,7 +14,7 @@
 //               the query heads of the kv head's group and over query tiles
 //               of 64 (causal: only tiles at or after the key tile), keeping
 //               dK and dV in TMEM; each step's dQ contribution is added to
-//               dQacc with fp32 reductions issued from registers.
+//               dQacc with a bulk fp32 reduction from shared memory.
 //   dq_convert  dQ = scale * dQacc -> bf16 [T, Hq, d].
 //
 // dkdv roles (320 threads):
@@ -24,9 +24,9 @@
 //              as A operands and dS^T also to shared memory (swizzled) as
 //              the B operand of dQ^T.
 //   warps 4-7  dQ drain: dQ^T rows (one TMEM lane = one head-dim column)
-//              added into dQacc with coalesced fp32 reductions.
+//              to shared memory, then one bulk reduce-add into dQacc.
 //   warp 8     MMA issuer; warp 9 TMA producer (K, V once; Q, dO per step
-//              into 4 stages, with that step's -L2 = -LSE * log2 e and D).
+//              into 3 stages, with that step's L2 = LSE * log2 e and D).
 // MMAs per step i (M = 128 keys; queries N = 64):
 //   S^T(i) = K Q_i^T and dP^T(i) = V dO_i^T          (SS, both K-major)
 //   dV += P^T(i) dO_i and dK += dS^T(i) Q_i           (TS, B MN-major)
@@ -47,7 +47,7 @@ namespace {
 constexpr int kThreads = 320;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
-constexpr int kQStages = 4;
+constexpr int kQStages = 3;
 
 template <int D>
 struct BwdCfg {
@@ -57,18 +57,17 @@ struct BwdCfg {
   static constexpr int Q_BOX = 64 * 64 * 2;       // 64 rows x 64 columns
   static constexpr int Q_TILE = NB * Q_BOX;
   static constexpr int DS_BYTES = 128 * 64 * 2;   // dS^T: 128 keys x 64 queries
+  static constexpr int DQ_BYTES = 64 * D * 4;     // fp32 dQ staging, [64][D]
   static constexpr int SIDE_BYTES = 528;          // L2[64], D[64], slope
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + KV_TILE;
   static constexpr int Q_OFF = V_OFF + KV_TILE;
   static constexpr int DO_OFF = Q_OFF + kQStages * Q_TILE;
   static constexpr int DS_OFF = DO_OFF + kQStages * Q_TILE;
-  static constexpr int SIDE_OFF = DS_OFF + 2 * DS_BYTES;
+  static constexpr int DQ_OFF = DS_OFF + 2 * DS_BYTES;
+  static constexpr int SIDE_OFF = DQ_OFF + DQ_BYTES;
   static constexpr int BAR_OFF = SIDE_OFF + kQStages * SIDE_BYTES;
-  static constexpr int SMEM_USED = BAR_OFF + 144;     // from a 1024-aligned base
-  // Launch size: the layout plus as much alignment slack as the per-block
-  // limit leaves; the kernel checks that the slack covers its base offset.
-  static constexpr int SMEM_BYTES = SMEM_USED + 1024 < 232448 ? SMEM_USED + 1024 : 232448;
+  static constexpr int SMEM_BYTES = BAR_OFF + 144 + 1024;
   static constexpr uint32_t DV_COL = 0, DK_COL = D;
   static constexpr uint32_t SB_COL0 = 256, PB_COL0 = 384;   // + 64 * buffer
 };
@@ -78,7 +77,7 @@ struct BwdBars {
   uint64_t q_full[kQStages], q_empty[kQStages];
   uint64_t sdp_full[2];
   uint64_t p_ready[2];       // per step parity: arrivals can never run a phase ahead
-  uint64_t dq_full, dq_free, dkdv_done;
+  uint64_t dq_full, dq_free, dqs_free, dqs_full, dkdv_done;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -184,10 +183,6 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  if ((int)(smem - smem_raw) + C::SMEM_USED > C::SMEM_BYTES) {   // uniform over the CTA
-    if (threadIdx.x == 0) record_status(p.status, FA_ERR_UNSUPPORTED);
-    return;
-  }
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::BAR_OFF);
   Side* side = reinterpret_cast<Side*>(smem + C::SIDE_OFF);
 
@@ -220,6 +215,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     mbar_init(&bars->p_ready[1], 4);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_free, 4);
+    mbar_init(&bars->dqs_free, 1);
+    mbar_init(&bars->dqs_full, 4);
     mbar_init(&bars->dkdv_done, 1);
     bars->abort_flag = 0;
     fence_mbarrier_init();
@@ -479,6 +476,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int q4 = warp & 3;
     const int c = 32 * q4 + lane;             // head-dim column of dQ^T
     const uint32_t lane_base = tmem + ((uint32_t)(32 * q4) << 16);
+    float* dqs = reinterpret_cast<float*>(smem + C::DQ_OFF);
     bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
       const int buf = it & 1;
@@ -496,16 +494,28 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->dq_free);
-      // fp32 add into the accumulator straight from registers: for each
-      // query the 32 lanes of a warp cover 32 consecutive head-dim columns,
-      // one coalesced 128-byte reduction per warp instruction.
+      if (!(ok = wait_warp(&bars->dqs_free, (it & 1) ^ 1, wc))) break;
       if (c < D) {
-        float* dst = p.dq_acc + ((long long)h * p.T + seq0 + q0) * D + c;
 #pragma unroll
-        for (int qq = 0; qq < 64; ++qq)
-          if (qq < nvalid) atomicAdd(dst + (long long)qq * D, __uint_as_float(r[qq]));
+        for (int qq = 0; qq < 64; ++qq) dqs[qq * D + c] = __uint_as_float(r[qq]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->dqs_full);
+      if (q4 == 0) {
+        if (!(ok = wait_warp(&bars->dqs_full, it & 1, wc))) break;
+        if (lane == 0) {
+          bulk_reduce_add_f32(p.dq_acc + ((long long)h * p.T + seq0 + q0) * D, dqs,
+                              (uint32_t)(nvalid * D * 4));
+          bulk_commit_group();
+          bulk_wait_group_read0();
+          mbar_arrive(&bars->dqs_free);
+        }
+        __syncwarp();
       }
     }
+    if (q4 == 0 && lane == 0) bulk_wait_group0();
+    __syncwarp();
     // dK epilogue
     if (ok) ok = wait_warp(&bars->dkdv_done, 0, wc);
     if (ok) {
