@@ -42,6 +42,7 @@ constexpr int kThreads = 320;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr float kTau = 8.0f;
+constexpr float kSpecSum = 256.0f;   // 2^kTau
 
 template <int D>
 struct FwdCfg {
@@ -277,11 +278,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       reg_fence32(s + 96);
       const int n0 = 128 * j;
       const bool need_mask = (CAUSAL && n0 + 127 > m0 + 128 * t) || (n0 + 128 > L);
-      // Row max over four independent chains of 3-input max (short
-      // dependency chains: one softmax warp per SM sub-partition at a time).
-      float mx[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
+      // Scores in the log2 domain (ALiBi: with the bias; masked: -inf).
       if (ALIBI) {
         const float base = slope2 * (float)(n0 - row);
 #pragma unroll
@@ -300,63 +297,82 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           if (key >= L || (CAUSAL && key > row)) s[c] = __float_as_uint(-INFINITY);
         }
       }
-#pragma unroll
-      for (int c = 0; c < 128; c += 8)
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          mx[i] = fmax3(mx[i], __uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1]));
-      float xmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
-      if (!ALIBI) xmax *= c2;
-      // lazy rescale: raise the reference only when the max grew past tau
-      const bool raise = xmax > m_ref + kTau;
-      const float m_new = raise ? xmax : m_ref;
-      const float alpha = raise ? ex2_approx(m_ref - m_new) : 1.f;
-      l *= alpha;
-      lr *= alpha;
-      if (j > 0 && __any_sync(0xffffffffu, raise)) {
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 16) {
-          uint32_t o[16];
-          tmem_ld16(tO + c0, o);
-          tmem_wait_ld();
-          reg_fence16(o);
-#pragma unroll
-          for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-          tmem_st16(tO + c0, o);
-        }
-      }
-      m_ref = m_new;
-      const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // p = 2^(x - m): packed f32x2 scale-and-subtract, MUFU exp2, and two
-      // sums (exact p; bf16-rounded p) in two independent packed chains each.
+      // p = 2^(x - m) with packed f32x2 scale-and-subtract and MUFU exp2;
+      // P is stored to TMEM as produced; returns the tile's sums of the
+      // exact p and of the bf16-rounded p the PV MMA sees.
       const uint64_t c2p = f2(c2, c2);
-      const uint64_t nmb = f2(-mb, -mb);
-      uint64_t acc[2] = {0, 0}, accr[2] = {0, 0};
+      auto exp_pass = [&](float mb, float& ts, float& tsr) {
+        const uint64_t nmb = f2(-mb, -mb);
+        uint64_t acc[2] = {0, 0}, accr[2] = {0, 0};
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t pk[16];
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const uint64_t xy = f2(__uint_as_float(s[32 * ch + 2 * c]), __uint_as_float(s[32 * ch + 2 * c + 1]));
-          const uint64_t e = ALIBI ? fadd2(xy, nmb) : ffma2(xy, c2p, nmb);
-          float e0, e1;
-          f2split(e, e0, e1);
-          const float p0 = ex2_approx(e0);
-          const float p1 = ex2_approx(e1);
-          acc[c & 1] = fadd2(acc[c & 1], f2(p0, p1));
-          pk[c] = pack_bf16x2(p0, p1);
-          accr[c & 1] = fadd2(accr[c & 1], f2(__uint_as_float(pk[c] << 16),
-                                               __uint_as_float(pk[c] & 0xFFFF0000u)));
+          for (int c = 0; c < 16; ++c) {
+            const uint64_t xy = f2(__uint_as_float(s[32 * ch + 2 * c]), __uint_as_float(s[32 * ch + 2 * c + 1]));
+            const uint64_t e = ALIBI ? fadd2(xy, nmb) : ffma2(xy, c2p, nmb);
+            float e0, e1;
+            f2split(e, e0, e1);
+            const float p0 = ex2_approx(e0);
+            const float p1 = ex2_approx(e1);
+            acc[c & 1] = fadd2(acc[c & 1], f2(p0, p1));
+            pk[c] = pack_bf16x2(p0, p1);
+            accr[c & 1] = fadd2(accr[c & 1], f2(__uint_as_float(pk[c] << 16),
+                                                 __uint_as_float(pk[c] & 0xFFFF0000u)));
+          }
+          tmem_st16(tS + 16 * ch, pk);
         }
-        tmem_st16(tS + 16 * ch, pk);
-      }
-      {
         float a0, a1, b0, b1;
         f2split(fadd2(acc[0], acc[1]), a0, a1);
         f2split(fadd2(accr[0], accr[1]), b0, b1);
-        l += a0 + a1;
-        lr += b0 + b1;
+        ts = a0 + a1;
+        tsr = b0 + b1;
+      };
+      // Speculative pass: once a row has a reference max, compute P with it
+      // directly.  If the tile's sum of p is at most 2^tau, no p exceeds 2^tau,
+      // i.e. no score exceeds the reference by more than tau, so no raise is
+      // due and the pass is exactly what the full path would produce.
+      float ts = 0.f, tsr = 0.f;
+      bool full = __any_sync(0xffffffffu, m_ref == -INFINITY);
+      if (!full) {
+        exp_pass(m_ref, ts, tsr);
+        full = __any_sync(0xffffffffu, !(ts <= kSpecSum));   // also catches inf / nan
+        if (full) tmem_wait_st();
       }
+      if (full) {
+        float mx[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 128; c += 8)
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            mx[i] = fmax3(mx[i], __uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1]));
+        float xmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
+        if (!ALIBI) xmax *= c2;
+        // lazy rescale: raise the reference only when the max grew past tau
+        const bool raise = xmax > m_ref + kTau;
+        const float m_new = raise ? xmax : m_ref;
+        const float alpha = raise ? ex2_approx(m_ref - m_new) : 1.f;
+        l *= alpha;
+        lr *= alpha;
+        if (j > 0 && __any_sync(0xffffffffu, raise)) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 16) {
+            uint32_t o[16];
+            tmem_ld16(tO + c0, o);
+            tmem_wait_ld();
+            reg_fence16(o);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st16(tO + c0, o);
+          }
+        }
+        m_ref = m_new;
+        exp_pass(m_ref == -INFINITY ? 0.f : m_ref, ts, tsr);
+      }
+      l += ts;
+      lr += tsr;
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
