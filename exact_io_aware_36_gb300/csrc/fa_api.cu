@@ -46,6 +46,8 @@ fa_status check_sizes(int B, int Hq, int Hkv, int N, int d, float scale,
   if (dtype == FA_FP32 && d > 128) return FA_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || !isfinite(scale)) return FA_ERR_UNSUPPORTED;
   if (B > 65535 || Hq > 65535) return FA_ERR_UNSUPPORTED;
+  // 1-D grids of (blocks per sequence) x heads x sequences must fit 2^31 - 1
+  if ((long long)((N + 127) / 128) * Hq * B >= (1ll << 31)) return FA_ERR_UNSUPPORTED;
   const long long dense = (long long)B * N;
   if (cu_seqlens == nullptr) {
     if (total_tokens != 0 && total_tokens != dense) return FA_ERR_SHAPE;

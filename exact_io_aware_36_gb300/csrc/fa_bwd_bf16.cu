@@ -188,9 +188,25 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int b = blockIdx.z;
-  const int g = blockIdx.y;                 // kv head
-  const int n0 = blockIdx.x * 128;          // key tile start within the sequence
+  // 1-D grid.  Dense batches: key tile slowest, so with a causal mask the
+  // first key tiles of every sequence and kv head (they meet the most query
+  // tiles) are launched first and the SMs are loaded longest-first.  Packed
+  // batches hold many sequences of different lengths: there the key tiles
+  // of one (sequence, kv head) are launched together instead, so they share
+  // its Q / dO stream through L2.
+  const int nkt = (p.N + 127) / 128;
+  int g, b, n0;
+  if (p.cu_seqlens) {
+    const int gb = (int)(blockIdx.x / (unsigned)nkt);
+    g = gb % p.Hkv;
+    b = gb / p.Hkv;
+    n0 = (int)(blockIdx.x % (unsigned)nkt) * 128;
+  } else {
+    const int gb = (int)(blockIdx.x % (unsigned)(p.Hkv * p.B));
+    g = gb % p.Hkv;
+    b = gb / p.Hkv;
+    n0 = (int)(blockIdx.x / (unsigned)(p.Hkv * p.B)) * 128;
+  }
   long long seq0;
   int L;
   if (!seq_bounds(p, b, &seq0, &L)) {
@@ -346,6 +362,15 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           mma_ts(tmem + C::DK_COL, tmem + C::PB_COL0 + 64 * buf + 8 * kk,
                  smem_desc_sw128(qb + kk * 2048, C::Q_BOX, 1024), ID_KV, (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars->q_empty[st]);
+      }
+      __syncwarp();
+      // dq_full(it) must not complete before the drain has seen dq_full(it-1)
+      // (a skipped phase would leave the drain waiting for good).  Steps
+      // it-1 < n-2 already waited for that drain before dP(it+1); the last
+      // step did not, so it waits here.
+      if (it >= 1 && it + 1 >= n_iter && !(ok = wait_warp(&bars->dq_free, (it - 1) & 1, wc))) break;
+      tc_fence_after();
+      if (lane == 0) {
         const uint32_t dsb = sdS + buf * C::DS_BYTES;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)   // dQ^T = K^T dS^T   (K = 128 keys)
@@ -563,7 +588,7 @@ int launch_dkdv(const AttnParams& p, cudaStream_t stream) {
   if (!r) r = make_tmap_bf16_3d(&tk, p.k, D, p.Hkv, p.T, 128);
   if (!r) r = make_tmap_bf16_3d(&tv, p.v, D, p.Hkv, p.T, 128);
   if (r) return r;
-  dim3 grid((p.N + 127) / 128, p.Hkv, p.B);
+  dim3 grid((unsigned)(((p.N + 127) / 128) * p.Hkv * p.B));
   kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, p);
   return (int)cudaGetLastError();
 }

@@ -84,9 +84,15 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int b = blockIdx.z;
-  const int h = blockIdx.y;
-  const int qb = CAUSAL ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+  // 1-D grid, query block slowest: with a causal mask the blocks far down
+  // the sequence (most K/V tiles) are all launched first, across every head
+  // and sequence, so the SMs are loaded longest-first and the tail is short.
+  const int nqb = (p.N + 255) / 256;
+  const int hb = (int)(blockIdx.x % (unsigned)(p.Hq * p.B));
+  const int qslot = (int)(blockIdx.x / (unsigned)(p.Hq * p.B));
+  const int h = hb % p.Hq;
+  const int b = hb / p.Hq;
+  const int qb = CAUSAL ? nqb - 1 - qslot : qslot;
 
   long long seq0;
   int L;
@@ -114,6 +120,14 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   }
   if (!tile1) nkv[1] = 0;
   const int nkv_max = max(nkv[0], nkv[1]);
+  // Step k of the K/V stream visits kv tile kvj(k).  With ALiBi the tiles go
+  // from the diagonal backwards: the positive slope makes scores grow toward
+  // the diagonal, so the first tile holds (nearly) the row max and the lazy
+  // rescale almost never fires.  Tile t is active on steps
+  // [k0[t], k0[t] + nkv[t]).
+  constexpr bool REV = ALIBI;
+  auto kvj = [&](int k) { return REV ? nkv_max - 1 - k : k; };
+  const int k0[2] = {REV ? nkv_max - nkv[0] : 0, REV ? nkv_max - nkv[1] : 0};
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -159,7 +173,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
     __syncwarp();
     int issued_k = 0, issued_v = 0;   // tiles whose loads were issued
-    for (int j = 0; j < nkv_max; ++j) {
+    for (int j = 0; j < nkv_max; ++j) {       // j: step index; kvj(j): kv tile
       const int sk = j % C::KS;
       if (!wait_warp(&bars->k_empty[sk], ((j / C::KS) & 1) ^ 1, wc)) break;
       if (lane == 0) {
@@ -167,7 +181,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
         for (int bx = 0; bx < C::NB; ++bx)
           tma_load_3d(smem + C::K_OFF + sk * C::TILE_BYTES + bx * C::BOX_BYTES, &tmK, bx * 64, kvh,
-                      (int)(seq0 + 128 * j), &bars->k_full[sk]);
+                      (int)(seq0 + 128 * kvj(j)), &bars->k_full[sk]);
       }
       __syncwarp();
       issued_k = j + 1;
@@ -178,7 +192,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
         for (int bx = 0; bx < C::NB; ++bx)
           tma_load_3d(smem + C::V_OFF + sv * C::TILE_BYTES + bx * C::BOX_BYTES, &tmV, bx * 64, kvh,
-                      (int)(seq0 + 128 * j), &bars->v_full[sv]);
+                      (int)(seq0 + 128 * kvj(j)), &bars->v_full[sv]);
       }
       __syncwarp();
       issued_v = j + 1;
@@ -207,8 +221,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tc_fence_after();
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
-        if (j >= 1 && j - 1 < nkv[t]) {
-          if (!(ok = wait_warp(&bars->p_full[t], (j - 1) & 1, wc))) break;
+        if (j >= 1 && j - 1 >= k0[t] && j - 1 < k0[t] + nkv[t]) {
+          if (!(ok = wait_warp(&bars->p_full[t], (j - 1 - k0[t]) & 1, wc))) break;
           tc_fence_after();
           if (lane == 0) {
             const uint32_t vbase = sV + sp * C::TILE_BYTES;
@@ -216,12 +230,12 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             for (int kk = 0; kk < 128 / 16; ++kk) {
               const uint64_t bdesc = smem_desc_sw128(vbase + kk * 2048, C::BOX_BYTES, 1024);
               mma_ts(tmem + colO[t], tmem + colS[t] + kk * 8, bdesc, IDESC_O,
-                     (j - 1 > 0 || kk > 0) ? 1u : 0u);
+                     (j - 1 > k0[t] || kk > 0) ? 1u : 0u);
             }
           }
           __syncwarp();
         }
-        if (j < nkv[t]) {
+        if (j >= k0[t] && j < k0[t] + nkv[t]) {
           if (lane == 0) {
             const uint32_t qbase = sQ + t * C::TILE_BYTES;
             const uint32_t kbase = sK + sj * C::TILE_BYTES;
@@ -263,7 +277,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     float l = 0.f;     // sum of p in fp32: gives the LSE
     float lr = 0.f;    // sum of the bf16-rounded p the PV MMA sees: normalises O
     bool ok = true;
-    for (int j = 0; j < nkv[t]; ++j) {
+    for (int j = 0; j < nkv[t]; ++j) {        // j: this tile's local step
       if (!(ok = wait_warp(&bars->s_full[t], j & 1, wc))) break;
       tc_fence_after();
       uint32_t s[128];
@@ -276,41 +290,40 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       reg_fence32(s + 32);
       reg_fence32(s + 64);
       reg_fence32(s + 96);
-      const int n0 = 128 * j;
+      const int n0 = 128 * kvj(k0[t] + j);
       const bool need_mask = (CAUSAL && n0 + 127 > m0 + 128 * t) || (n0 + 128 > L);
-      // Scores in the log2 domain (ALiBi: with the bias; masked: -inf).
-      if (ALIBI) {
-        const float base = slope2 * (float)(n0 - row);
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          float x = fmaf(__uint_as_float(s[c]), c2, fmaf(slope2, (float)c, base));
-          if (need_mask) {
-            const int key = n0 + c;
-            if (key >= L || (CAUSAL && key > row)) x = -INFINITY;
-          }
-          s[c] = __float_as_uint(x);
-        }
-      } else if (need_mask) {
+      // Masked scores become -inf (raw scores stay in s; the scale and the
+      // ALiBi bias are applied where they are consumed).
+      if (need_mask) {
 #pragma unroll
         for (int c = 0; c < 128; ++c) {
           const int key = n0 + c;
           if (key >= L || (CAUSAL && key > row)) s[c] = __float_as_uint(-INFINITY);
         }
       }
+      // ALiBi bias of column c in log2 units: slope2 * (n0 + c - row).
+      const float base = ALIBI ? slope2 * (float)(n0 - row) : 0.f;
       // p = 2^(x - m) with packed f32x2 scale-and-subtract and MUFU exp2;
       // P is stored to TMEM as produced; returns the tile's sums of the
       // exact p and of the bf16-rounded p the PV MMA sees.
       const uint64_t c2p = f2(c2, c2);
       auto exp_pass = [&](float mb, float& ts, float& tsr) {
         const uint64_t nmb = f2(-mb, -mb);
+        const uint64_t step = f2(2.f * slope2, 2.f * slope2);
         uint64_t acc[2] = {0, 0}, accr[2] = {0, 0};
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           uint32_t pk[16];
+          // ALiBi: bias - m for the pair (c, c+1), exact at the chunk start
+          // and advanced by 2 * slope2 per pair (16 steps at most).
+          uint64_t bm = ALIBI ? f2(fmaf(slope2, (float)(32 * ch), base - mb),
+                                   fmaf(slope2, (float)(32 * ch + 1), base - mb))
+                              : nmb;
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             const uint64_t xy = f2(__uint_as_float(s[32 * ch + 2 * c]), __uint_as_float(s[32 * ch + 2 * c + 1]));
-            const uint64_t e = ALIBI ? fadd2(xy, nmb) : ffma2(xy, c2p, nmb);
+            const uint64_t e = ffma2(xy, c2p, bm);
+            if (ALIBI) bm = fadd2(bm, step);
             float e0, e1;
             f2split(e, e0, e1);
             const float p0 = ex2_approx(e0);
@@ -343,11 +356,22 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         float mx[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
+        if (ALIBI) {       // max of s * c2 + bias
 #pragma unroll
-        for (int c = 0; c < 128; c += 8)
+          for (int c = 0; c < 128; c += 8)
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            mx[i] = fmax3(mx[i], __uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1]));
+            for (int i = 0; i < 4; ++i) {
+              const int cc = c + 2 * i;
+              mx[i] = fmax3(mx[i], fmaf(__uint_as_float(s[cc]), c2, fmaf(slope2, (float)cc, base)),
+                            fmaf(__uint_as_float(s[cc + 1]), c2, fmaf(slope2, (float)(cc + 1), base)));
+            }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 128; c += 8)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              mx[i] = fmax3(mx[i], __uint_as_float(s[c + 2 * i]), __uint_as_float(s[c + 2 * i + 1]));
+        }
         float xmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
         if (!ALIBI) xmax *= c2;
         // lazy rescale: raise the reference only when the max grew past tau
@@ -439,7 +463,7 @@ int launch_impl(const AttnParams& p, cudaStream_t stream) {
   if (!r) r = make_tmap_bf16_3d(&tk, p.k, D, p.Hkv, p.T, 128);
   if (!r) r = make_tmap_bf16_3d(&tv, p.v, D, p.Hkv, p.T, 128);
   if (r) return r;
-  dim3 grid((p.N + 255) / 256, p.Hq, p.B);
+  dim3 grid((unsigned)(((p.N + 255) / 256) * p.Hq * p.B));
   kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
   return (int)cudaGetLastError();
 }
