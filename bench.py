@@ -63,6 +63,23 @@ def dist_info():
     return world, rank, local
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The job's time is the slowest rank's: all-reduce MAX over the ranks
+    (the only collective; replicas exchange no data)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank_step: float, ms_per_step: float, world: int) -> float:
+    """Whole-job TFLOP/s: every rank runs the same replica (weak scaling)."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def flops_per_step(w: I.Workload, seqlens) -> dict:
     pairs = I.attended_pairs(w, seqlens)
     return {"pairs": pairs, "fwd": 4.0 * w.d * pairs, "bwd": 10.0 * w.d * pairs,
@@ -236,13 +253,9 @@ def run_ours(args, world, rank, local):
     st = fa.fa_check_device_error(sp)
     if st:
         raise fa.FAError(st, "timed region")
-    total_ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(start.elapsed_time(end), world, dev)
     ms_step = total_ms / args.steps
-    value = world * fl["total"] / (ms_step * 1e-3) / 1e12
+    value = job_throughput(fl["total"], ms_step, world)
 
     kern_ms = {}
     for j, name in enumerate(names[:nev - 1]):
