@@ -41,6 +41,9 @@ R6  Causal: key j visible to query i iff j <= i, positions local to the
     sequence; query and key lengths are equal per sequence.
 R7  A row with no visible key (cannot occur under R6) gets O = 0, LSE = -inf.
 R8  No dropout (the usage contract's example passes dropout_p = 0.0).
+R9  Sliding window (named only, among the mask variants of the usage contract
+    table): a causal band, key j visible to query i iff i - window <= j <= i;
+    window None (or < 0) means no window; window requires causal.
 """
 from __future__ import annotations
 
@@ -57,13 +60,23 @@ def _f64(x):
     return np.asarray(x, dtype=np.float64)
 
 
-def head_scores(q, k, scale, causal, slope=None):
+def _window(window, causal):
+    if window is None or window < 0:
+        return None
+    if not causal:
+        raise ValueError("a sliding window needs causal=True (R9)")
+    return int(window)
+
+
+def head_scores(q, k, scale, causal, slope=None, window=None):
     """Scores of one (sequence, head): S = scale * q k^T + bias, masked.
 
     [FA1 note] Key design 1, S = QK^T / sqrt(d) with ``scale`` in place of
     1/sqrt(d) (usage contract: softmax_scale).  ALiBi bias per R4, added after
-    scaling (R1).  Causal mask per R6: masked entries are -inf.
+    scaling (R1).  Causal mask per R6, sliding window per R9: masked entries
+    are -inf.
     """
+    window = _window(window, causal)
     q = _f64(q)
     k = _f64(k)
     L = q.shape[0]
@@ -74,6 +87,8 @@ def head_scores(q, k, scale, causal, slope=None):
         S = S - float(slope) * (i - j)
     if causal:
         vis = np.arange(k.shape[0])[None, :] <= np.arange(L)[:, None]
+        if window is not None:
+            vis &= np.arange(k.shape[0])[None, :] >= np.arange(L)[:, None] - window
         S = np.where(vis, S, -np.inf)
     return S
 
@@ -92,20 +107,20 @@ def _softmax_rows(S):
     return P, lse
 
 
-def head_forward(q, k, v, scale, causal, slope=None):
+def head_forward(q, k, v, scale, causal, slope=None, window=None):
     """O and LSE of one (sequence, head), materialising S and P.
 
     [FA1 note] Key design 1: P = softmax(S), O = P V.  Key design 2's table:
     L = m + log l is saved per row for the backward (R3).
     Returns (O, LSE, P).
     """
-    S = head_scores(q, k, scale, causal, slope)
+    S = head_scores(q, k, scale, causal, slope, window)
     P, lse = _softmax_rows(S)
     O = P @ _f64(v)
     return O, lse, P
 
 
-def head_backward(q, k, v, do, scale, causal, slope=None):
+def head_backward(q, k, v, do, scale, causal, slope=None, window=None):
     """dQ, dK, dV of one (sequence, head) from the materialised P.
 
     [FA1 note] Key design 3: dV = P^T dO; dP = dO V^T; D_i = rowsum(P o dP)
@@ -117,7 +132,7 @@ def head_backward(q, k, v, do, scale, causal, slope=None):
     k = _f64(k)
     v = _f64(v)
     do = _f64(do)
-    O, lse, P = head_forward(q, k, v, scale, causal, slope)
+    O, lse, P = head_forward(q, k, v, scale, causal, slope, window)
     dV = P.T @ do
     dP = do @ v.T
     D = (P * dP).sum(axis=1)
@@ -144,7 +159,7 @@ def _slope(alibi_slopes, h):
 
 
 def attention_forward(q, k, v, scale, causal, cu_seqlens=None, alibi_slopes=None,
-                      heads=None, seqs=None):
+                      heads=None, seqs=None, window=None):
     """O [T, Hq, d] and LSE [Hq, T] of packed multi-head attention.
 
     Sequences are the segments [cu[b], cu[b+1]) of the token axis ([Memory-wall
@@ -160,14 +175,14 @@ def attention_forward(q, k, v, scale, causal, cu_seqlens=None, alibi_slopes=None
         for h in (range(Hq) if heads is None else heads):
             g = h // group
             o, lse, _ = head_forward(q[s:e, h], k[s:e, g], v[s:e, g], scale, causal,
-                                     _slope(alibi_slopes, h))
+                                     _slope(alibi_slopes, h), window)
             O[s:e, h] = o
             LSE[h, s:e] = lse
     return O, LSE
 
 
 def attention_backward(q, k, v, do, scale, causal, cu_seqlens=None, alibi_slopes=None,
-                       heads=None, seqs=None):
+                       heads=None, seqs=None, window=None):
     """dQ, dK, dV (plus O, LSE, D) of packed multi-head attention.
 
     dK and dV of kv head g sum the contributions of its query heads (R5).
@@ -188,7 +203,7 @@ def attention_backward(q, k, v, do, scale, causal, cu_seqlens=None, alibi_slopes
             g = h // group
             dq, dk, dv, o, lse, dd = head_backward(
                 q[s:e, h], k[s:e, g], v[s:e, g], do[s:e, h], scale, causal,
-                _slope(alibi_slopes, h))
+                _slope(alibi_slopes, h), window)
             dQ[s:e, h] = dq
             dK[s:e, g] += dk
             dV[s:e, g] += dv
@@ -203,7 +218,7 @@ def attention_backward(q, k, v, do, scale, causal, cu_seqlens=None, alibi_slopes
 # against the definition above (exactness, FA1 Theorem 1).
 # --------------------------------------------------------------------------
 
-def online_softmax_forward(q, k, v, scale, causal, slope=None, block_q=1, block_k=1):
+def online_softmax_forward(q, k, v, scale, causal, slope=None, block_q=1, block_k=1, window=None):
     """Forward by the mergeable (m, l, O) state, FA1 loop order.
 
     [FA1 note] Key design 1: K/V blocks in the outer loop, Q blocks in the
@@ -220,7 +235,7 @@ def online_softmax_forward(q, k, v, scale, causal, slope=None, block_q=1, block_
     O = np.zeros((Lq, v.shape[1]))
     m = np.full(Lq, -np.inf)
     l = np.zeros(Lq)
-    S_all = head_scores(q, k, scale, causal, slope)   # tiles are read from here
+    S_all = head_scores(q, k, scale, causal, slope, window)   # tiles are read from here
     for ks in range(0, Lk, block_k):
         ke = min(ks + block_k, Lk)
         for qs in range(0, Lq, block_q):
@@ -233,15 +248,17 @@ def online_softmax_forward(q, k, v, scale, causal, slope=None, block_q=1, block_
             P_t = np.zeros_like(S)
             P_t[ok] = np.exp(S[ok] - m_t[ok, None])
             l_t = P_t.sum(axis=1)
-            m_old, l_old, O_old = m[qs:qe], l[qs:qe], O[qs:qe]
-            m_new = np.maximum(m_old, np.where(ok, m_t, -np.inf))
+            # rows that see no key of this tile merge nothing and keep their state
+            rows = np.arange(qs, qe)[ok]
+            m_old, l_old, O_old = m[rows], l[rows], O[rows]
+            m_t, l_t, PV_t = m_t[ok], l_t[ok], (P_t @ v[ks:ke])[ok]
+            m_new = np.maximum(m_old, m_t)
             a_old = np.where(np.isfinite(m_old), np.exp(m_old - m_new), 0.0)
-            a_new = np.where(ok, np.exp(np.where(ok, m_t, 0.0) - m_new), 0.0)
+            a_new = np.exp(m_t - m_new)
             l_new = a_old * l_old + a_new * l_t
-            num = (a_old * l_old)[:, None] * O_old + a_new[:, None] * (P_t @ v[ks:ke])
-            O[qs:qe] = num / l_new[:, None]
-            m[qs:qe] = m_new
-            l[qs:qe] = l_new
+            O[rows] = ((a_old * l_old)[:, None] * O_old + a_new[:, None] * PV_t) / l_new[:, None]
+            m[rows] = m_new
+            l[rows] = l_new
     lse = np.where(l > 0, m + np.log(np.where(l > 0, l, 1.0)), -np.inf)
     return O, lse
 
@@ -289,7 +306,7 @@ def _seq_of(cu, t):
     return b, int(cu[b]), int(cu[b + 1])
 
 
-def forward_rows(q, k, v, scale, causal, rows, cu_seqlens=None, alibi_slopes=None):
+def forward_rows(q, k, v, scale, causal, rows, cu_seqlens=None, alibi_slopes=None, window=None):
     """O and LSE at sampled (token t, query head h) rows.
 
     Row i of Key design 1's definition needs only q_i and the sequence's keys:
@@ -308,14 +325,17 @@ def forward_rows(q, k, v, scale, causal, rows, cu_seqlens=None, alibi_slopes=Non
         if alibi_slopes is not None:
             srow = srow - float(alibi_slopes[h]) * (i - np.arange(e - s, dtype=np.float64))
         if causal:
-            srow = np.where(np.arange(e - s) <= i, srow, -np.inf)
+            vis = np.arange(e - s) <= i
+            if _window(window, causal) is not None:
+                vis &= np.arange(e - s) >= i - window
+            srow = np.where(vis, srow, -np.inf)
         P, lse = _softmax_rows(srow[None, :])
         outO.append((P @ _f64(v[s:e, g]))[0])
         outL.append(lse[0])
     return np.array(outO), np.array(outL)
 
 
-def head_row_stats(q, k, v, do, scale, causal, s, e, h, g, slope=None, chunk=1024):
+def head_row_stats(q, k, v, do, scale, causal, s, e, h, g, slope=None, chunk=1024, window=None):
     """LSE_i and D_i = dO_i . O_i of every query row of one (sequence, head).
 
     Computed in row chunks (each chunk materialises its rows of S), so whole
@@ -334,7 +354,10 @@ def head_row_stats(q, k, v, do, scale, causal, s, e, h, g, slope=None, chunk=102
         if slope is not None:
             S = S - slope * (i - j)
         if causal:
-            S = np.where(j <= i, S, -np.inf)
+            vis = j <= i
+            if _window(window, causal) is not None:
+                vis &= j >= i - window
+            S = np.where(vis, S, -np.inf)
         P, lse[r0:r1] = _softmax_rows(S)
         if D is not None:
             D[r0:r1] = (_f64(do[s + r0:s + r1, h]) * (P @ vv)).sum(axis=1)
@@ -342,7 +365,7 @@ def head_row_stats(q, k, v, do, scale, causal, s, e, h, g, slope=None, chunk=102
 
 
 def backward_query_rows(q, k, v, do, scale, causal, rows, cu_seqlens=None,
-                        alibi_slopes=None):
+                        alibi_slopes=None, window=None):
     """dQ at sampled (token t, query head h) rows.
 
     Row i of Key design 3: P_i from its scores, dP_i = dO_i V^T,
@@ -361,7 +384,10 @@ def backward_query_rows(q, k, v, do, scale, causal, rows, cu_seqlens=None,
         if alibi_slopes is not None:
             srow = srow - float(alibi_slopes[h]) * (i - np.arange(e - s, dtype=np.float64))
         if causal:
-            srow = np.where(np.arange(e - s) <= i, srow, -np.inf)
+            vis = np.arange(e - s) <= i
+            if _window(window, causal) is not None:
+                vis &= np.arange(e - s) >= i - window
+            srow = np.where(vis, srow, -np.inf)
         P, _ = _softmax_rows(srow[None, :])
         P = P[0]
         o = P @ vv
@@ -374,7 +400,7 @@ def backward_query_rows(q, k, v, do, scale, causal, rows, cu_seqlens=None,
 
 
 def backward_key_rows(q, k, v, do, scale, causal, rows, cu_seqlens=None,
-                      alibi_slopes=None, stats_cache=None):
+                      alibi_slopes=None, stats_cache=None, window=None):
     """dK and dV at sampled (token t, kv head g) rows.
 
     Column j of Key design 3's formulas: dV_j = sum_i P_ij dO_i and
@@ -397,7 +423,7 @@ def backward_key_rows(q, k, v, do, scale, causal, rows, cu_seqlens=None,
             slope = _slope(alibi_slopes, h)
             if (b, h) not in stats_cache:
                 stats_cache[(b, h)] = head_row_stats(q, k, v, do, scale, causal,
-                                                     s, e, h, g, slope)
+                                                     s, e, h, g, slope, window=window)
             lse, D = stats_cache[(b, h)]
             qq = _f64(q[s:e, h])
             dd = _f64(do[s:e, h])
@@ -406,7 +432,10 @@ def backward_key_rows(q, k, v, do, scale, causal, rows, cu_seqlens=None,
             if slope is not None:
                 scol = scol - slope * (i - j)
             if causal:
-                scol = np.where(i >= j, scol, -np.inf)
+                vis = i >= j
+                if _window(window, causal) is not None:
+                    vis &= i <= j + window
+                scol = np.where(vis, scol, -np.inf)
             Pcol = np.where(np.isfinite(scol), np.exp(scol - lse), 0.0)
             dPcol = dd @ _f64(v[t, g])
             dScol = Pcol * (dPcol - D)

@@ -312,3 +312,115 @@ def test_sampled_rows_equal_full_oracle():
     for n, (t, g) in enumerate(krows):
         np.testing.assert_allclose(dk_r[n], dk[t, g], atol=1e-12)
         np.testing.assert_allclose(dv_r[n], dv[t, g], atol=1e-12)
+
+
+# ------------------------------------------------------------ sliding window
+
+@pytest.mark.parametrize("w", [0, 1, 5, 28])
+def test_window_zero_query_gives_band_mean(w):
+    """Q = 0: row i averages V over the band [max(0, i - w), i] and LSE_i is
+    ln(band length)."""
+    L, d = 29, 8
+    v = rnd(70, L, d)
+    O, lse, _ = A.head_forward(np.zeros((L, d)), rnd(71, L, d), v, 0.3, True, None, w)
+    for i in range(L):
+        lo = max(0, i - w)
+        np.testing.assert_allclose(O[i], v[lo:i + 1].mean(0), rtol=0, atol=1e-13)
+        assert abs(lse[i] - np.log(i - lo + 1)) < 1e-13
+
+
+def test_window_zero_is_the_diagonal_and_wide_window_is_causal():
+    L, d = 21, 8
+    q, k, v = rnd(72, L, d), rnd(73, L, d), rnd(74, L, d)
+    O, lse, _ = A.head_forward(q, k, v, 0.4, True, None, 0)
+    np.testing.assert_allclose(O, v, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse, 0.4 * (q * k).sum(1), rtol=0, atol=1e-14)
+    O1, l1, _ = A.head_forward(q, k, v, 0.4, True, 0.2, L - 1)
+    O2, l2, _ = A.head_forward(q, k, v, 0.4, True, 0.2)
+    np.testing.assert_allclose(O1, O2, atol=0)
+    np.testing.assert_allclose(l1, l2, atol=0)
+    with pytest.raises(ValueError):
+        A.head_forward(q, k, v, 0.4, False, None, 3)
+
+
+def test_window_ignores_keys_outside_the_band():
+    """Rows whose band excludes key j are unchanged when k_j and v_j change."""
+    L, d, w, j = 40, 8, 6, 10
+    q, k, v = rnd(75, L, d), rnd(76, L, d), rnd(77, L, d)
+    O1, l1, _ = A.head_forward(q, k, v, 0.5, True, None, w)
+    k2, v2 = k.copy(), v.copy()
+    k2[j] += 3.0
+    v2[j] -= 2.0
+    O2, l2, _ = A.head_forward(q, k2, v2, 0.5, True, None, w)
+    outside = [i for i in range(L) if not (i - w <= j <= i)]
+    inside = [i for i in range(L) if i - w <= j <= i]
+    np.testing.assert_allclose(O1[outside], O2[outside], atol=0)
+    assert np.abs(O1[inside] - O2[inside]).max() > 1e-3
+
+
+@pytest.mark.parametrize("w,bq,bk", [(3, 1, 1), (7, 3, 5), (16, 40, 7)])
+def test_window_online_recurrence_equals_two_pass(w, bq, bk):
+    L, d = 40, 8
+    q, k, v = rnd(78, L, d, scale=2.0), rnd(79, L, d), rnd(80, L, d)
+    O_ref, lse_ref, _ = A.head_forward(q, k, v, 0.4, True, 0.3, w)
+    O, lse = A.online_softmax_forward(q, k, v, 0.4, True, 0.3, bq, bk, window=w)
+    np.testing.assert_allclose(O, O_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+
+
+def test_window_gradients_match_finite_differences():
+    q, k, v, do, cu, slopes = _fd_case(True, True, 2, 1, [7, 4])
+    scale, w = 0.6, 2
+
+    def f(q_, k_, v_):
+        O, _ = A.attention_forward(q_, k_, v_, scale, True, cu, slopes, window=w)
+        return float((do * O).sum())
+
+    dq, dk, dv, *_ = A.attention_backward(q, k, v, do, scale, True, cu, slopes, window=w)
+    h = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp = x.copy(); xp[idx] += h
+            xm = x.copy(); xm[idx] -= h
+            args_p = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+            args_m = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+            num[idx] = (f(*args_p) - f(*args_m)) / (2 * h)
+        assert np.max(np.abs(num - g)) / np.max(np.abs(g)) <= 1e-6, name
+
+
+def test_window_matches_torch_float64_sdpa():
+    torch = pytest.importorskip("torch")
+    L, H, d, w, scale = 33, 2, 16, 5, 0.25
+    q, k, v, do = rnd(81, L, H, d), rnd(82, L, H, d), rnd(83, L, H, d), rnd(84, L, H, d)
+    dq, dk, dv, O, lse, _ = A.attention_backward(q, k, v, do, scale, True, window=w)
+    tq, tk, tv = (torch.tensor(x.transpose(1, 0, 2)[None], requires_grad=True) for x in (q, k, v))
+    i = torch.arange(L)[:, None]
+    j = torch.arange(L)[None, :]
+    mask = torch.zeros(L, L, dtype=torch.float64).masked_fill((j > i) | (j < i - w), float("-inf"))
+    out = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, scale=scale)
+    out.backward(torch.tensor(do.transpose(1, 0, 2)[None]))
+    np.testing.assert_allclose(O, out[0].detach().numpy().transpose(1, 0, 2), atol=1e-12)
+    for a, t in ((dq, tq), (dk, tk), (dv, tv)):
+        np.testing.assert_allclose(a, t.grad[0].numpy().transpose(1, 0, 2), atol=1e-11)
+
+
+def test_window_sampled_rows_equal_full_oracle():
+    lens = [70, 33, 101]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T, Hq, Hkv, d, w = cu[-1], 4, 2, 16, 9
+    q, k, v, do = rnd(85, T, Hq, d), rnd(86, T, Hkv, d), rnd(87, T, Hkv, d), rnd(88, T, Hq, d)
+    slopes = I.alibi_slopes(Hq).astype(np.float64)
+    dq, dk, dv, O, lse, _ = A.attention_backward(q, k, v, do, 0.25, True, cu, slopes, window=w)
+    rows = [(0, 0), (69, 3), (70, 1), (102, 2), (T - 1, 0), (150, 3)]
+    O_r, lse_r = A.forward_rows(q, k, v, 0.25, True, rows, cu, slopes, window=w)
+    dq_r = A.backward_query_rows(q, k, v, do, 0.25, True, rows, cu, slopes, window=w)
+    for n, (t, h) in enumerate(rows):
+        np.testing.assert_allclose(O_r[n], O[t, h], atol=1e-13)
+        assert abs(lse_r[n] - lse[h, t]) < 1e-13
+        np.testing.assert_allclose(dq_r[n], dq[t, h], atol=1e-13)
+    krows = [(0, 0), (69, 1), (70, 0), (T - 1, 1), (120, 1)]
+    dk_r, dv_r = A.backward_key_rows(q, k, v, do, 0.25, True, krows, cu, slopes, window=w)
+    for n, (t, g) in enumerate(krows):
+        np.testing.assert_allclose(dk_r[n], dk[t, g], atol=1e-12)
+        np.testing.assert_allclose(dv_r[n], dv[t, g], atol=1e-12)

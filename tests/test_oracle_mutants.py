@@ -16,11 +16,11 @@ _orig_backward = A.head_backward
 _orig_softmax = A._softmax_rows
 
 
-def scores_alibi_sign(q, k, scale, causal, slope=None):
-    return _orig_scores(q, k, scale, causal, None if slope is None else -slope)
+def scores_alibi_sign(q, k, scale, causal, slope=None, window=None):
+    return _orig_scores(q, k, scale, causal, None if slope is None else -slope, window)
 
 
-def scores_causal_off_by_one(q, k, scale, causal, slope=None):
+def scores_causal_off_by_one(q, k, scale, causal, slope=None, window=None):
     S = _orig_scores(q, k, scale, False, slope)
     if causal:
         L = S.shape[0]
@@ -30,13 +30,13 @@ def scores_causal_off_by_one(q, k, scale, causal, slope=None):
     return S
 
 
-def scores_scale_twice(q, k, scale, causal, slope=None):
-    return _orig_scores(q, k, scale * scale, causal, slope) if scale != 1.0 else \
-        _orig_scores(q, k, 0.5, causal, slope)
+def scores_scale_twice(q, k, scale, causal, slope=None, window=None):
+    return _orig_scores(q, k, scale * scale, causal, slope, window) if scale != 1.0 else \
+        _orig_scores(q, k, 0.5, causal, slope, window)
 
 
-def scores_bias_scaled(q, k, scale, causal, slope=None):
-    return _orig_scores(q, k, scale, causal, None if slope is None else slope * scale)
+def scores_bias_scaled(q, k, scale, causal, slope=None, window=None):
+    return _orig_scores(q, k, scale, causal, None if slope is None else slope * scale, window)
 
 
 def softmax_log2(S):
@@ -45,9 +45,9 @@ def softmax_log2(S):
 
 
 def _backward_mutant(kind):
-    def f(q, k, v, do, scale, causal, slope=None):
+    def f(q, k, v, do, scale, causal, slope=None, window=None):
         q, k, v, do = (np.asarray(x, np.float64) for x in (q, k, v, do))
-        O, lse, Pm = A.head_forward(q, k, v, scale, causal, slope)
+        O, lse, Pm = A.head_forward(q, k, v, scale, causal, slope, window)
         dP = do @ v.T
         D = (Pm * dP).sum(1)
         if kind == "D_dropped":
@@ -70,7 +70,12 @@ def _backward_mutant(kind):
     return f
 
 
+def scores_window_off_by_one(q, k, scale, causal, slope=None, window=None):
+    return _orig_scores(q, k, scale, causal, slope, None if window is None else window - 1)
+
+
 MUTANTS = {
+    "window_off_by_one": ("head_scores", scores_window_off_by_one),
     "alibi_sign": ("head_scores", scores_alibi_sign),
     "causal_off_by_one": ("head_scores", scores_causal_off_by_one),
     "scale_twice": ("head_scores", scores_scale_twice),
@@ -96,6 +101,7 @@ PINS = [
     P.test_alibi_sign_and_index_by_row_shift,
     P.test_alibi_huge_slope_picks_diagonal,
     lambda: P.test_matches_torch_float64_sdpa_and_autograd(True, True, 4, 2),
+    lambda: P.test_window_zero_query_gives_band_mean(5),
 ]
 
 
