@@ -195,6 +195,13 @@ fa_status fa_bwd_stage(int stage, const void* q, const void* k, const void* v, c
                   workspace_bytes, stream);
 }
 
+fa_status fa_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return FA_ERR_UNSUPPORTED;
+  unsigned int* status = status_ptr();
+  if (!status) return FA_ERR_CUDA;
+  return fa::launch_selftest_wait(status, limit_ns, stream) == 0 ? FA_OK : FA_ERR_CUDA;
+}
+
 fa_status fa_check_device_error(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
   unsigned int* p = status_ptr();

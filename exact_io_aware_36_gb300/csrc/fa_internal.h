@@ -43,5 +43,6 @@ struct AttnParams {
 int launch_fwd_fp32(const AttnParams& p, void* stream);
 int launch_fwd_bf16(const AttnParams& p, void* stream);
 int launch_bwd_bf16(const AttnParams& p, void* stream, int stage);   // stage < 0: all
+int launch_selftest_wait(unsigned int* status, unsigned long long limit_ns, void* stream);
 
 }  // namespace fa

@@ -126,12 +126,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 struct WaitCtx {
   volatile int* abort_flag;   // shared memory, 0 = running
   unsigned int* status;       // global per-device status word
+  unsigned long long limit_ns = kWaitLimitNs;
 };
 
 // Slow path of wait_warp, kept out of line so the timer state does not add
 // register pressure to the loops that wait.
 static __device__ __noinline__ bool wait_warp_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                            unsigned int* status) {
+                                            unsigned int* status, unsigned long long limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     bool ok = mbar_try_wait(bar, parity);
@@ -139,7 +140,7 @@ static __device__ __noinline__ bool wait_warp_slow(uint64_t* bar, uint32_t parit
     int bad = 0;
     if ((threadIdx.x & 31) == 0) {
       if (*abort_flag) bad = 1;
-      else if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      else if (globaltimer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         record_status(status, FA_ERR_DEVICE_TIMEOUT);
         bad = 1;
@@ -153,7 +154,7 @@ static __device__ __noinline__ bool wait_warp_slow(uint64_t* bar, uint32_t parit
 // All 32 lanes must call it; the result is warp-uniform.
 __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
   if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-  return wait_warp_slow(bar, parity, w.abort_flag, w.status);
+  return wait_warp_slow(bar, parity, w.abort_flag, w.status, w.limit_ns);
 }
 
 // Bounded wait that ignores the abort flag, used while unwinding: copies and

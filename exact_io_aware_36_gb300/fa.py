@@ -25,7 +25,7 @@ STATUS = {
     5: "FA_ERR_WORKSPACE", 6: "FA_ERR_CUDA", 7: "FA_ERR_DEVICE_TIMEOUT", 8: "FA_ERR_CU_SEQLENS",
 }
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_stage", "fa_bwd_workspace_size", "fa_check_device_error",
-           "fa_status_string", "fa_version", "fa_bwd_static_scratch")
+           "fa_status_string", "fa_version", "fa_bwd_static_scratch", "fa_selftest_wait_timeout")
 FA_BWD_PREPROCESS, FA_BWD_DKDV, FA_BWD_DQ_CONVERT = 0, 1, 2
 
 
@@ -116,6 +116,15 @@ def fa_bwd_static_scratch(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, sca
 
 def fa_bwd_workspace_size(B, Hq, N, d, total_tokens) -> int:
     return load().fa_bwd_workspace_size(B, Hq, N, d, total_tokens)
+
+
+def fa_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
+    """Launch one block whose bounded wait can never complete (see fa.h)."""
+    lib = load()
+    fn = lib.fa_selftest_wait_timeout
+    fn.argtypes = [ctypes.c_ulonglong, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    return fn(limit_ns, stream)
 
 
 def fa_check_device_error(stream=None) -> int:

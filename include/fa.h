@@ -187,6 +187,17 @@ fa_status fa_bwd_static_scratch(const void* q, const void* k, const void* v, con
  */
 fa_status fa_check_device_error(void* stream);
 
+/*
+ * Diagnostic: launches (asynchronously, on `stream`) one block whose bounded
+ * pipeline wait can never be satisfied, with a limit of `limit_ns`
+ * nanoseconds (1 ns .. 10 s).  The block records FA_ERR_DEVICE_TIMEOUT in
+ * the device status word and returns; nothing hangs and nothing faults.  It
+ * exercises the same wait the attention kernels use, so a caller can check
+ * that a stalled pipeline surfaces through fa_check_device_error() on its
+ * device, and that the context is usable afterwards.
+ */
+fa_status fa_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
+
 /* Static description of a status code (never NULL). */
 const char* fa_status_string(fa_status status);
 
