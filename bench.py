@@ -100,13 +100,14 @@ def source_hash(name: str) -> str:
     return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if
-    the kernel's source is unchanged since the counters were taken."""
+def ncu_traffic(workload: str, kernel: str):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload` from the
+    committed ncu summary, or None when there is none or when any source the
+    kernel is built from has changed since the counters were taken."""
     try:
         with open(TRAFFIC_FILE) as f:
-            rec = json.load(f)[kernel]
-        if source_hash(rec["source"]) != rec["source_sha256_16"]:
+            rec = json.load(f)[workload][kernel]
+        if any(source_hash(n) != h for n, h in rec["sources_sha256_16"].items()):
             return None
         return rec["bytes_per_launch"]
     except Exception:
@@ -268,10 +269,10 @@ def run_ours(args, world, rank, local):
         roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(ach / peak, 4),
                 "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
-                "traffic": ncu_traffic(dom)}
+                "traffic": ncu_traffic(w.name, dom)}
     else:
         roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s",
-                "frac": None, "traffic": ncu_traffic(dom)}
+                "frac": None, "traffic": ncu_traffic(w.name, dom)}
     per_kernel = {n: {"ms": round(kern_ms[n], 4),
                       "tflops": round(kern_flops[n] / (kern_ms[n] * 1e-3) / 1e12, 1)
                       if n in kern_flops else None,
