@@ -60,9 +60,16 @@ fa_status check_sizes(int B, int Hq, int Hkv, int N, int d, float scale,
   return FA_OK;
 }
 
+// Window argument -> band width: < 0 means none; a band that reaches back
+// over the whole longest sequence (window >= N - 1) masks nothing beyond the
+// causal mask, so it is run as unbanded.
+int band_width(int window, int N) { return (window < 0 || window >= N - 1) ? fa::kNoWindow : window; }
+
 fa::AttnParams base_params(int B, int Hq, int Hkv, int N, int d, float scale, int causal,
-                           const int32_t* cu_seqlens, long long T, const float* alibi) {
+                           int window, const int32_t* cu_seqlens, long long T,
+                           const float* alibi) {
   fa::AttnParams p = {};
+  p.window = band_width(window, N);
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -100,12 +107,13 @@ const char* fa_status_string(fa_status s) {
 }
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
-                 int Hkv, int N, int d, float scale, int causal, const int32_t* cu_seqlens,
-                 long long total_tokens, const float* alibi_slopes, fa_dtype dtype,
-                 fa_dtype o_dtype, void* stream) {
+                 int Hkv, int N, int d, float scale, int causal, int window,
+                 const int32_t* cu_seqlens, long long total_tokens, const float* alibi_slopes,
+                 fa_dtype dtype, fa_dtype o_dtype, void* stream) {
   long long T = 0;
   fa_status st = check_sizes(B, Hq, Hkv, N, d, scale, cu_seqlens, total_tokens, dtype, false, &T);
   if (st != FA_OK) return st;
+  if (window >= 0 && !causal) return FA_ERR_UNSUPPORTED;
   if (o_dtype != FA_FP32 && !(o_dtype == FA_BF16 && dtype == FA_BF16)) return FA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
   if (dtype == FA_BF16 && (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)))
@@ -115,7 +123,8 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     return FA_ERR_ALIGN;
   if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_ALIGN;
   if (T == 0 || B == 0 || N == 0) return FA_OK;
-  fa::AttnParams p = base_params(B, Hq, Hkv, N, d, scale, causal, cu_seqlens, T, alibi_slopes);
+  fa::AttnParams p = base_params(B, Hq, Hkv, N, d, scale, causal, window, cu_seqlens, T,
+                                 alibi_slopes);
   p.q = q;
   p.k = k;
   p.v = v;
@@ -136,14 +145,18 @@ size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, long long total_tokens
 
 static fa_status bwd_impl(int stage, const void* q, const void* k, const void* v, const void* o,
                           const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
-                          int Hq, int Hkv, int N, int d, float scale, int causal,
+                          int Hq, int Hkv, int N, int d, float scale, int causal, int window,
                           const int32_t* cu_seqlens, long long total_tokens,
                           const float* alibi_slopes, fa_dtype dtype, fa_dtype o_dtype,
-                          void* workspace, size_t workspace_bytes, void* stream) {
+                          int deterministic, void* workspace, size_t workspace_bytes,
+                          void* stream) {
   long long T = 0;
   fa_status st = check_sizes(B, Hq, Hkv, N, d, scale, cu_seqlens, total_tokens, dtype, true, &T);
   if (st != FA_OK) return st;
   if (o_dtype != FA_FP32 && o_dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+  if (window >= 0 && !causal) return FA_ERR_UNSUPPORTED;
+  if (deterministic != 0 && deterministic != 1) return FA_ERR_UNSUPPORTED;
+  if (deterministic) return FA_ERR_UNSUPPORTED;
   if (stage < -1 || stage > 2) return FA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
@@ -153,7 +166,9 @@ static fa_status bwd_impl(int stage, const void* q, const void* k, const void* v
   const size_t need = fa_bwd_workspace_size(B, Hq, N, d, T);
   if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_ALIGN;
-  fa::AttnParams p = base_params(B, Hq, Hkv, N, d, scale, causal, cu_seqlens, T, alibi_slopes);
+  fa::AttnParams p = base_params(B, Hq, Hkv, N, d, scale, causal, window, cu_seqlens, T,
+                                 alibi_slopes);
+  p.deterministic = deterministic;
   p.q = q;
   p.k = k;
   p.v = v;
@@ -175,24 +190,26 @@ static fa_status bwd_impl(int stage, const void* q, const void* k, const void* v
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
                  const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
-                 int d, float scale, int causal, const int32_t* cu_seqlens,
+                 int d, float scale, int causal, int window, const int32_t* cu_seqlens,
                  long long total_tokens, const float* alibi_slopes, fa_dtype dtype,
-                 fa_dtype o_dtype, void* workspace, size_t workspace_bytes, void* stream) {
-  return bwd_impl(-1, q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal,
-                  cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype, workspace,
-                  workspace_bytes, stream);
+                 fa_dtype o_dtype, int deterministic, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  return bwd_impl(-1, q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal, window,
+                  cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype, deterministic,
+                  workspace, workspace_bytes, stream);
 }
 
 fa_status fa_bwd_stage(int stage, const void* q, const void* k, const void* v, const void* o,
                        const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
-                       int Hq, int Hkv, int N, int d, float scale, int causal,
+                       int Hq, int Hkv, int N, int d, float scale, int causal, int window,
                        const int32_t* cu_seqlens, long long total_tokens,
                        const float* alibi_slopes, fa_dtype dtype, fa_dtype o_dtype,
-                       void* workspace, size_t workspace_bytes, void* stream) {
+                       int deterministic, void* workspace, size_t workspace_bytes,
+                       void* stream) {
   if (stage < 0 || stage > 2) return FA_ERR_UNSUPPORTED;
   return bwd_impl(stage, q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal,
-                  cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype, workspace,
-                  workspace_bytes, stream);
+                  window, cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype, deterministic,
+                  workspace, workspace_bytes, stream);
 }
 
 fa_status fa_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {

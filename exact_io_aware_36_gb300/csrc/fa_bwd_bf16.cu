@@ -175,7 +175,8 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const AttnParams p)
 }
 
 // ---------------------------------------------------------------------- dkdv
-template <int D, bool CAUSAL, bool ALIBI>
+// BAND: causal band (sliding window p.window); only with CAUSAL.
+template <int D, bool CAUSAL, bool ALIBI, bool BAND>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -214,9 +215,14 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     return;
   }
   if (n0 >= L) return;
+  // Query tiles that see this key tile: all of them without a mask; under
+  // the causal mask those from the diagonal on, and with a sliding window w
+  // only those up to query n0 + 127 + w.
+  const int W = p.window;
   const int nqt_all = (L + 63) / 64;
   const int qt0 = CAUSAL ? n0 / 64 : 0;
-  const int nqt = nqt_all - qt0;            // query tiles per head (>= 1)
+  const int qt_end = BAND ? min(nqt_all, (n0 + 127 + W) / 64 + 1) : nqt_all;
+  const int nqt = qt_end - qt0;             // query tiles per head (>= 1)
   const int n_iter = p.group * nqt;
 
   if (threadIdx.x == 0) {
@@ -412,7 +418,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       if (!(ok = wait_warp(&bars->sdp_full[buf], (it >> 1) & 1, wc))) break;
       tc_fence_after();
       const Side* sd = side + st;
-      const bool need_mask = (CAUSAL && q0 < n0 + 127) || !key_ok;
+      const bool need_mask = (CAUSAL && q0 < n0 + 127) || (BAND && q0 + 63 > n0 + W) || !key_ok;
       // x = S^T * scale * log2(e) + slope2 * (key - q0) + nL2[q]: the bias
       // term is split into a per-thread part (key - q0, exact integer) and a
       // per-query part folded into nL2 by the producer.
@@ -447,8 +453,8 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
             if (need_mask) {
               const int q = q0 + 32 * half + ql;
-              if (!key_ok || (CAUSAL && key > q)) p0 = 0.f;
-              if (!key_ok || (CAUSAL && key > q + 1)) p1 = 0.f;
+              if (!key_ok || (CAUSAL && key > q) || (BAND && q > key + W)) p0 = 0.f;
+              if (!key_ok || (CAUSAL && key > q + 1) || (BAND && q + 1 > key + W)) p1 = 0.f;
             }
             const uint64_t pp = f2(p0, p1);
             const uint64_t dsd = fmul2(pp, fsub2(f2(__uint_as_float(dp[ql]), __uint_as_float(dp[ql + 1])),
@@ -576,10 +582,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   }
 }
 
-template <int D, bool CAUSAL, bool ALIBI>
+template <int D, bool CAUSAL, bool ALIBI, bool BAND>
 int launch_dkdv(const AttnParams& p, cudaStream_t stream) {
   using C = BwdCfg<D>;
-  auto kern = bwd_dkdv_kernel<D, CAUSAL, ALIBI>;
+  auto kern = bwd_dkdv_kernel<D, CAUSAL, ALIBI, BAND>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return (int)e;
   CUtensorMap tq, tk, tv, tdo;
@@ -604,8 +610,12 @@ int launch_stages(const AttnParams& p, cudaStream_t stream, int stage) {
   if (stage < 0 || stage == 1) {
     int r;
     const bool alibi = p.alibi != nullptr;
-    if (p.causal) r = alibi ? launch_dkdv<D, true, true>(p, stream) : launch_dkdv<D, true, false>(p, stream);
-    else r = alibi ? launch_dkdv<D, false, true>(p, stream) : launch_dkdv<D, false, false>(p, stream);
+    if (p.causal && p.window != kNoWindow)
+      r = alibi ? launch_dkdv<D, true, true, true>(p, stream) : launch_dkdv<D, true, false, true>(p, stream);
+    else if (p.causal)
+      r = alibi ? launch_dkdv<D, true, true, false>(p, stream) : launch_dkdv<D, true, false, false>(p, stream);
+    else
+      r = alibi ? launch_dkdv<D, false, true, false>(p, stream) : launch_dkdv<D, false, false, false>(p, stream);
     if (r) return r;
   }
   if (stage < 0 || stage == 2) {

@@ -49,8 +49,8 @@ void* scratch_ptr() {
 extern "C" fa_status fa_bwd_static_scratch(
     const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
     void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, float scale, int causal,
-    const int32_t* cu_seqlens, long long total_tokens, const float* alibi_slopes, fa_dtype dtype,
-    fa_dtype o_dtype, void* stream) {
+    int window, const int32_t* cu_seqlens, long long total_tokens, const float* alibi_slopes,
+    fa_dtype dtype, fa_dtype o_dtype, int deterministic, void* stream) {
   // The size check comes first and needs no GPU: a problem whose D and dQ
   // accumulator do not fit the fixed array is refused before anything runs.
   const long long T = cu_seqlens ? total_tokens : (long long)B * N;
@@ -61,7 +61,7 @@ extern "C" fa_status fa_bwd_static_scratch(
   // Everything the kernels read from the scratch is written by the same call
   // first: D by the preprocess kernel, and the dQ accumulator is zeroed
   // there too, so the previous call's contents never leak into this one.
-  return fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal, cu_seqlens,
-                total_tokens, alibi_slopes, dtype, o_dtype, ws,
+  return fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal, window,
+                cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype, deterministic, ws,
                 (size_t)FA_BWD_STATIC_SCRATCH_BYTES, stream);
 }

@@ -73,7 +73,8 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-template <int D, bool CAUSAL, bool ALIBI>
+// BAND: causal band (sliding window p.window); only with CAUSAL.
+template <int D, bool CAUSAL, bool ALIBI, bool BAND>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
@@ -112,22 +113,34 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int m0 = qb * 256;
   if (m0 >= L) return;                       // uniform: nothing to do
   const bool tile1 = m0 + 128 < L;
-  int nkv[2];
+  // Query tile t (rows [r0, r0 + 128)) needs kv tiles lo[t] .. hi[t]: all of
+  // them without a mask; under the causal mask those up to the diagonal, and
+  // with a sliding window w only those from row r0 - w on.
+  const int W = p.window;
+  int lo[2], hi[2], nkv[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
-    const int rows_end = min(m0 + 128 * (t + 1), L);
-    nkv[t] = CAUSAL ? (rows_end + 127) / 128 : (L + 127) / 128;
+    const int r0 = m0 + 128 * t;
+    const int rows_end = min(r0 + 128, L);
+    lo[t] = BAND ? max(0, r0 - W) / 128 : 0;
+    hi[t] = CAUSAL ? (rows_end - 1) / 128 : (L - 1) / 128;
+    nkv[t] = hi[t] - lo[t] + 1;
   }
-  if (!tile1) nkv[1] = 0;
-  const int nkv_max = max(nkv[0], nkv[1]);
-  // Step k of the K/V stream visits kv tile kvj(k).  With ALiBi the tiles go
-  // from the diagonal backwards: the positive slope makes scores grow toward
-  // the diagonal, so the first tile holds (nearly) the row max and the lazy
-  // rescale almost never fires.  Tile t is active on steps
-  // [k0[t], k0[t] + nkv[t]).
+  if (!tile1) {
+    nkv[1] = 0;
+    lo[1] = lo[0];
+    hi[1] = hi[0];
+  }
+  // The K/V stream covers kv tiles lo[0] .. hi[1] (tile 1's range starts and
+  // ends no earlier than tile 0's, and the two overlap or touch).  Step k
+  // visits kv tile kvj(k).  With ALiBi the tiles go from the diagonal
+  // backwards: the positive slope makes scores grow toward the diagonal, so
+  // the first tile holds (nearly) the row max and the lazy rescale almost
+  // never fires.  Tile t is active on steps [k0[t], k0[t] + nkv[t]).
+  const int nkv_max = hi[1] - lo[0] + 1;
   constexpr bool REV = ALIBI;
-  auto kvj = [&](int k) { return REV ? nkv_max - 1 - k : k; };
-  const int k0[2] = {REV ? nkv_max - nkv[0] : 0, REV ? nkv_max - nkv[1] : 0};
+  auto kvj = [&](int k) { return REV ? hi[1] - k : lo[0] + k; };
+  const int k0[2] = {REV ? hi[1] - hi[0] : 0, REV ? 0 : lo[1] - lo[0]};
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -291,14 +304,17 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       reg_fence32(s + 64);
       reg_fence32(s + 96);
       const int n0 = 128 * kvj(k0[t] + j);
-      const bool need_mask = (CAUSAL && n0 + 127 > m0 + 128 * t) || (n0 + 128 > L);
+      const int r0 = m0 + 128 * t;
+      const bool need_mask = (CAUSAL && n0 + 127 > r0) || (BAND && n0 < r0 + 127 - W) || (n0 + 128 > L);
       // Masked scores become -inf (raw scores stay in s; the scale and the
-      // ALiBi bias are applied where they are consumed).
+      // ALiBi bias are applied where they are consumed).  A row can meet a
+      // tile that is wholly outside its band; its scores are then all -inf,
+      // its p all 0, and its state unchanged.
       if (need_mask) {
 #pragma unroll
         for (int c = 0; c < 128; ++c) {
           const int key = n0 + c;
-          if (key >= L || (CAUSAL && key > row)) s[c] = __float_as_uint(-INFINITY);
+          if (key >= L || (CAUSAL && key > row) || (BAND && key < row - W)) s[c] = __float_as_uint(-INFINITY);
         }
       }
       // ALiBi bias of column c in log2 units: slope2 * (n0 + c - row).
@@ -451,10 +467,10 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   }
 }
 
-template <int D, bool CAUSAL, bool ALIBI>
+template <int D, bool CAUSAL, bool ALIBI, bool BAND>
 int launch_impl(const AttnParams& p, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  auto kern = fwd_bf16_kernel<D, CAUSAL, ALIBI>;
+  auto kern = fwd_bf16_kernel<D, CAUSAL, ALIBI, BAND>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return (int)e;
@@ -468,17 +484,21 @@ int launch_impl(const AttnParams& p, cudaStream_t stream) {
   return (int)cudaGetLastError();
 }
 
+template <int D>
+int launch_masks(const AttnParams& p, cudaStream_t stream) {
+  const bool alibi = p.alibi != nullptr;
+  if (p.causal && p.window != kNoWindow)
+    return alibi ? launch_impl<D, true, true, true>(p, stream) : launch_impl<D, true, false, true>(p, stream);
+  if (p.causal)
+    return alibi ? launch_impl<D, true, true, false>(p, stream) : launch_impl<D, true, false, false>(p, stream);
+  return alibi ? launch_impl<D, false, true, false>(p, stream) : launch_impl<D, false, false, false>(p, stream);
+}
+
 }  // namespace
 
 int launch_fwd_bf16(const AttnParams& p, void* stream_) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  const bool alibi = p.alibi != nullptr;
-  if (p.d == 128) {
-    if (p.causal) return alibi ? launch_impl<128, true, true>(p, stream) : launch_impl<128, true, false>(p, stream);
-    return alibi ? launch_impl<128, false, true>(p, stream) : launch_impl<128, false, false>(p, stream);
-  }
-  if (p.causal) return alibi ? launch_impl<64, true, true>(p, stream) : launch_impl<64, true, false>(p, stream);
-  return alibi ? launch_impl<64, false, true>(p, stream) : launch_impl<64, false, false>(p, stream);
+  return p.d == 128 ? launch_masks<128>(p, stream) : launch_masks<64>(p, stream);
 }
 
 }  // namespace fa

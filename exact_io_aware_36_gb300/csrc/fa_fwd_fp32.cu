@@ -62,6 +62,7 @@ fwd_fp32_kernel(AttnParams p) {
   const float c2 = p.scale_log2;
   const float slope2 = p.alibi ? p.alibi[h] * kLog2e : 0.f;
   const int n_keys = p.causal ? row + 1 : L;
+  const int key_lo = p.causal ? max(0, row - p.window) : 0;   // sliding-window band start
 
   float m = -INFINITY;
   float l = 0.f;
@@ -69,7 +70,7 @@ fwd_fp32_kernel(AttnParams p) {
 #pragma unroll
   for (int i = 0; i < kCols; ++i) acc[i] = 0.f;
 
-  for (int k0 = 0; k0 < n_keys; k0 += 32) {
+  for (int k0 = key_lo; k0 < n_keys; k0 += 32) {
     const int j = k0 + lane;
     float x = -INFINITY;
     if (j < n_keys) {

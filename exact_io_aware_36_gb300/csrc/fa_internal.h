@@ -15,6 +15,10 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Band width that stands for "no sliding window": larger than any sequence
+// (lengths are below 2^30), small enough that key + window cannot overflow.
+constexpr int kNoWindow = 1 << 30;
+
 struct AttnParams {
   const void* q;
   const void* k;
@@ -34,6 +38,9 @@ struct AttnParams {
   int B, Hq, Hkv, N, d;
   int group;                   // Hq / Hkv
   int causal;
+  int window;                  // causal band: key j visible to query i iff
+                               // i - window <= j <= i; kNoWindow when unbanded
+  int deterministic;           // backward: dQ by its own kernel, no atomics
   int o_f32;                    // o stored as fp32 (else the input dtype)
   float scale;
   float scale_log2;            // scale * log2(e)

@@ -54,10 +54,10 @@ def load(path: Optional[str] = None):
         raise FAError(6, f"libfa not built ({p} missing); run exact_io_aware_36_gb300.build")
     lib = ctypes.CDLL(p)
     vp, i, f, ll, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong, ctypes.c_size_t
-    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, ll, vp, i, i, vp]
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, ll, vp, i, i, vp]
     lib.fa_fwd.restype = i
-    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, ll, vp, i,
-                           i, vp, sz, vp]
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, ll, vp,
+                           i, i, i, vp, sz, vp]
     lib.fa_bwd.restype = i
     lib.fa_bwd_stage.argtypes = [i] + lib.fa_bwd.argtypes
     lib.fa_bwd_stage.restype = i
@@ -76,42 +76,45 @@ def load(path: Optional[str] = None):
 
 # ------------------------------------------------------------ raw C entry points
 
-def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, cu_seqlens, total_tokens,
+def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, causal, window, cu_seqlens, total_tokens,
            alibi_slopes, dtype, o_dtype, stream) -> int:
-    return load().fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, int(causal), cu_seqlens,
-                         total_tokens, alibi_slopes, dtype, o_dtype, stream)
+    return load().fa_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, int(causal), int(window),
+                         cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype, stream)
 
 
-def fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal, cu_seqlens,
-           total_tokens, alibi_slopes, dtype, o_dtype, workspace, workspace_bytes, stream) -> int:
+def fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal, window, cu_seqlens,
+           total_tokens, alibi_slopes, dtype, o_dtype, deterministic, workspace, workspace_bytes,
+           stream) -> int:
     return load().fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, int(causal),
-                         cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype, workspace,
-                         workspace_bytes, stream)
+                         int(window), cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype,
+                         int(deterministic), workspace, workspace_bytes, stream)
 
 
-def fa_bwd_stage(stage, q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal,
-                 cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype, workspace,
+def fa_bwd_stage(stage, q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal, window,
+                 cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype, deterministic, workspace,
                  workspace_bytes, stream) -> int:
     return load().fa_bwd_stage(stage, q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale,
-                               int(causal), cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype,
-                               workspace, workspace_bytes, stream)
+                               int(causal), int(window), cu_seqlens, total_tokens, alibi_slopes,
+                               dtype, o_dtype, int(deterministic), workspace, workspace_bytes,
+                               stream)
 
 
 FA_BWD_STATIC_SCRATCH_BYTES = 64 << 20
 
 
 def fa_bwd_static_scratch(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal,
-                          cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype, stream) -> int:
+                          window, cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype,
+                          deterministic, stream) -> int:
     """fa_bwd without a workspace argument, for callers that cannot allocate
     device memory: the scratch lives in a fixed array of
     FA_BWD_STATIC_SCRATCH_BYTES inside the library (see include/fa.h)."""
     lib = load()
     fn = lib.fa_bwd_static_scratch
     if fn.restype is not ctypes.c_int or not fn.argtypes:
-        fn.argtypes = lib.fa_bwd.argtypes[:21] + [ctypes.c_void_p]
+        fn.argtypes = lib.fa_bwd.argtypes[:23] + [ctypes.c_void_p]
         fn.restype = ctypes.c_int
-    return fn(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, int(causal), cu_seqlens,
-              total_tokens, alibi_slopes, dtype, o_dtype, stream)
+    return fn(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, int(causal), int(window),
+              cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype, int(deterministic), stream)
 
 
 def fa_bwd_workspace_size(B, Hq, N, d, total_tokens) -> int:
@@ -173,14 +176,15 @@ def _dtype_code(dt):
 
 def attention_forward(q, k, v, *, causal: bool, scale: Optional[float] = None, cu_seqlens=None,
                       max_seqlen: Optional[int] = None, batch: Optional[int] = None,
-                      alibi_slopes=None, out=None, lse=None, out_dtype=None, stream=None,
-                      check: bool = False):
+                      alibi_slopes=None, window: Optional[int] = None, out=None, lse=None,
+                      out_dtype=None, stream=None, check: bool = False):
     """O, LSE = attention(q, k, v) through ``fa_fwd``.
 
     q: [T, Hq, d], k/v: [T, Hkv, d] (bf16 or fp32, contiguous, on the GPU).
     Dense batches pass ``batch`` (T = batch * N); packed batches pass int32
     ``cu_seqlens`` [B+1] and ``max_seqlen``.  Returns (o [T, Hq, d] of
     ``out_dtype`` (default: ``out``'s dtype, else q's), lse float32 [Hq, T]).
+    ``window`` w (causal only): query i sees keys i - w .. i; None: no window.
     """
     import torch
     T, B, Hq, Hkv, N, d = _sizes(q, k, cu_seqlens, max_seqlen, batch)
@@ -194,8 +198,8 @@ def attention_forward(q, k, v, *, causal: bool, scale: Optional[float] = None, c
     if lse is None:
         lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
     st = fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, N, d, float(scale),
-                causal, _ptr(cu_seqlens), T, _ptr(alibi_slopes), dtype, _dtype_code(out.dtype),
-                _stream(stream))
+                causal, -1 if window is None else window, _ptr(cu_seqlens), T,
+                _ptr(alibi_slopes), dtype, _dtype_code(out.dtype), _stream(stream))
     _check(st, "fa_fwd")
     if check:
         _check(fa_check_device_error(_stream(stream)), "fa_fwd (device)")
@@ -204,11 +208,14 @@ def attention_forward(q, k, v, *, causal: bool, scale: Optional[float] = None, c
 
 def attention_backward(q, k, v, o, dO, lse, *, causal: bool, scale: Optional[float] = None,
                        cu_seqlens=None, max_seqlen: Optional[int] = None,
-                       batch: Optional[int] = None, alibi_slopes=None, workspace=None,
-                       dq=None, dk=None, dv=None, stream=None, check: bool = False):
+                       batch: Optional[int] = None, alibi_slopes=None,
+                       window: Optional[int] = None, deterministic: bool = False,
+                       workspace=None, dq=None, dk=None, dv=None, stream=None,
+                       check: bool = False):
     """dQ, dK, dV through ``fa_bwd`` (bf16).  ``workspace`` (uint8 device
     tensor of at least ``fa_bwd_workspace_size`` bytes) is allocated when
-    not given."""
+    not given.  ``window`` as in attention_forward; ``deterministic`` selects
+    the backward whose results do not vary from run to run."""
     import torch
     T, B, Hq, Hkv, N, d = _sizes(q, k, cu_seqlens, max_seqlen, batch)
     if q.dtype != torch.bfloat16:
@@ -222,8 +229,9 @@ def attention_backward(q, k, v, o, dO, lse, *, causal: bool, scale: Optional[flo
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     st = fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq), _ptr(dk),
-                _ptr(dv), B, Hq, Hkv, N, d, float(scale), causal, _ptr(cu_seqlens), T,
-                _ptr(alibi_slopes), FA_BF16, _dtype_code(o.dtype), _ptr(workspace),
+                _ptr(dv), B, Hq, Hkv, N, d, float(scale), causal,
+                -1 if window is None else window, _ptr(cu_seqlens), T, _ptr(alibi_slopes),
+                FA_BF16, _dtype_code(o.dtype), deterministic, _ptr(workspace),
                 workspace.numel(), _stream(stream))
     _check(st, "fa_bwd")
     if check:

@@ -34,7 +34,7 @@ from typing import Optional
 import numpy as np
 
 __all__ = [
-    "Workload", "WORKLOADS", "workload", "make_inputs", "small_case",
+    "Workload", "WORKLOADS", "EXTRA_WORKLOADS", "workload", "make_inputs", "small_case",
     "bf16_round", "bf16_bits", "bf16_from_bits", "alibi_slopes",
     "attended_pairs",
 ]
@@ -62,6 +62,12 @@ class Workload:
     seqlen_range: Optional[tuple] = None
     seqlens: Optional[tuple] = None   # explicit packed lengths (tests)
     note: str = ""
+    window: Optional[int] = None      # causal band: query i sees keys i-window .. i
+
+    @property
+    def window_arg(self) -> int:
+        """The C ABI's window argument (-1: none)."""
+        return -1 if self.window is None else int(self.window)
 
     @property
     def varlen(self) -> bool:
@@ -92,21 +98,29 @@ WORKLOADS = {
         alibi=True, note="GQA 32/4 with ALiBi, causal, B=2 N=8192 d=128"),
 }
 
+# Further workloads for the rows beyond the five above: each is checked and
+# measured the same way but is not one of the five.
+EXTRA_WORKLOADS = {
+    "swa_32k": Workload(
+        "swa_32k", "bf16", causal=True, B=1, Hq=32, Hkv=8, N=32768, d=128, window=4095,
+        note="sliding window 4096 keys (causal band), GQA 32/8, B=1 N=32768 d=128"),
+}
+
 
 def workload(name: str) -> Workload:
-    return WORKLOADS[name]
+    return WORKLOADS[name] if name in WORKLOADS else EXTRA_WORKLOADS[name]
 
 
 def small_case(dtype="bf16", causal=True, B=1, Hq=2, Hkv=2, N=128, d=64,
                alibi=False, seqlens=None, qk_gain=1.0, backward=True,
-               name="small") -> Workload:
+               name="small", window=None) -> Workload:
     """A small workload for parity tests (explicit packed lengths allowed)."""
     if seqlens is not None:
         seqlens = tuple(int(x) for x in seqlens)
         B = len(seqlens)
         N = max(seqlens) if seqlens else 0
     return Workload(name, dtype, causal, B, Hq, Hkv, N, d, backward=backward,
-                    alibi=alibi, qk_gain=qk_gain, seqlens=seqlens)
+                    alibi=alibi, qk_gain=qk_gain, seqlens=seqlens, window=window)
 
 
 def bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -147,12 +161,17 @@ def _seqlens(w: Workload, rng: np.random.Generator) -> np.ndarray:
 def attended_pairs(w: Workload, seqlens=None) -> int:
     """Number of (query, key) pairs the workload attends, over heads and sequences.
 
-    Causal: L(L+1)/2 per sequence and query head; otherwise L*L.
+    Causal: L(L+1)/2 per sequence and query head; otherwise L*L.  With a
+    window w, query i attends min(i, w) + 1 keys: the band's area is
+    (w+1)(w+2)/2 + (L-w-1)(w+1) once L > w + 1.
     """
     if seqlens is None:
         seqlens = make_seqlens(w)
     L = np.asarray(seqlens, dtype=np.int64)
     per = L * (L + 1) // 2 if w.causal else L * L
+    if w.causal and w.window is not None and w.window >= 0:
+        b = np.int64(w.window) + 1
+        per = np.where(L > b, b * (b + 1) // 2 + (L - b) * b, per)
     return int(per.sum()) * w.Hq
 
 

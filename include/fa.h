@@ -10,8 +10,11 @@
  * ("FlashAttention: Faster Attention Without Dropping a Single Interaction",
  * Key design 1, the S/P/O definition; Key design 2, the saved statistic
  * L = m + log l).  B_h[i,j] = -slope_h * (i - j) when ALiBi slopes are given,
- * else 0; with causal != 0, S_ij = -inf for j > i.  The bias is added after
- * scaling and is not scaled.
+ * else 0; with causal != 0, S_ij = -inf for j > i, and with a sliding window
+ * w >= 0 also for j < i - w (the causal band i - w <= j <= i; the sliding
+ * window is named among the mask variants in the Usage contract table of
+ * "FlashAttention: Faster Attention Without Dropping a Single Interaction").
+ * The bias is added after scaling and is not scaled.
  * The backward recomputes P from LSE tile by tile (Key design 3):
  *     dV = P^T dO,  dP = dO V^T,  D_i = dO_i . O_i,  dS = P o (dP - D),
  *     dQ = scale * dS K,  dK = scale * dS^T Q,
@@ -79,6 +82,10 @@ typedef enum { FA_BF16 = 0, FA_FP32 = 1 } fa_dtype;
  *   d            head dimension: bf16 d in {64, 128}; fp32 1 <= d <= 128
  *   scale        softmax scale (> 0, finite), usually 1/sqrt(d)
  *   causal       0 or 1
+ *   window       sliding window w: key j visible to query i iff
+ *                i - w <= j <= i.  < 0: no window.  w >= 0 requires
+ *                causal == 1 (else FA_ERR_UNSUPPORTED); w = 0 lets each
+ *                query see only its own key; w >= N - 1 equals plain causal.
  *   cu_seqlens   device int32 [B+1] or NULL (dense)
  *   total_tokens T; for dense batches 0 or B*N
  *   alibi_slopes device float32 [Hq] or NULL
@@ -91,7 +98,7 @@ typedef enum { FA_BF16 = 0, FA_FP32 = 1 } fa_dtype;
  * kernel (bf16 operands, fp32 accumulation and softmax).
  */
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                 int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                 int B, int Hq, int Hkv, int N, int d, float scale, int causal, int window,
                  const int32_t* cu_seqlens, long long total_tokens,
                  const float* alibi_slopes, fa_dtype dtype, fa_dtype o_dtype,
                  void* stream);
@@ -99,35 +106,48 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 /*
  * Bytes of device workspace fa_bwd needs: D (float32 [Hq, T]) and the dQ
  * accumulator (float32 [Hq, T, d]), each 256-byte aligned.  T is
- * total_tokens when > 0, else B*N.  Returns 0 for invalid sizes.
+ * total_tokens when > 0, else B*N.  Returns 0 for invalid sizes.  The
+ * deterministic backward uses only the first part (D); this size serves
+ * both.
  */
 size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, long long total_tokens);
 
 /*
  * Backward: from q, k, v, the forward's o (element type o_dtype) and lse,
  * and dO, writes dq ([T, Hq, d]), dk and dv ([T, Hkv, d]), all bf16.  Same
- * size arguments as fa_fwd.  `workspace` (device, >= fa_bwd_workspace_size
- * bytes, 256-byte aligned, contents irrelevant on entry) is scratch owned by
- * the caller; it
- * must not be used by anything else until the call completes on `stream`.
- * dQ is accumulated with float32 reductions in an order that is not fixed,
- * so dq may differ in the last bits from run to run.  Only FA_BF16.
+ * size, mask and window arguments as fa_fwd.  `workspace` (device,
+ * >= fa_bwd_workspace_size bytes, 256-byte aligned, contents irrelevant on
+ * entry) is scratch owned by the caller; it must not be used by anything
+ * else until the call completes on `stream`.
+ *   deterministic  0: dQ is accumulated with float32 reductions in an order
+ *                  that is not fixed, so dq may differ in the last bits from
+ *                  run to run.  1: a separate kernel computes dQ per query
+ *                  tile without atomics (two more MMAs per attended pair);
+ *                  dq, dk and dv are then bit-identical from run to run
+ *                  (the same page, Limitations, "Numerical exactness, low
+ *                  precision, and reproducibility": a deterministic backward
+ *                  is an option and is slower).  Other values:
+ *                  FA_ERR_UNSUPPORTED.
+ * Only FA_BF16.
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
                  const void* dO, const float* lse, void* dq, void* dk, void* dv,
-                 int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                 int B, int Hq, int Hkv, int N, int d, float scale, int causal, int window,
                  const int32_t* cu_seqlens, long long total_tokens,
                  const float* alibi_slopes, fa_dtype dtype, fa_dtype o_dtype,
-                 void* workspace, size_t workspace_bytes, void* stream);
+                 int deterministic, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * One stage of fa_bwd, with fa_bwd's arguments, so a caller can time or
  * schedule the stages separately.  fa_bwd == the three stages in order on
  * one stream:
  *   FA_BWD_PREPROCESS  D = rowsum(dO o O) and the dQ accumulator zeroed
- *                      (both in the workspace)
+ *                      (both in the workspace; deterministic: D only)
  *   FA_BWD_DKDV        dk, dv, and dQ accumulated in the workspace
- *   FA_BWD_DQ_CONVERT  dq = scale * accumulator, as bf16
+ *                      (deterministic: dk and dv only)
+ *   FA_BWD_DQ_CONVERT  dq = scale * accumulator, as bf16 (deterministic:
+ *                      dq computed by its own kernel from q, k, v, dO, lse
+ *                      and D, one query tile per block)
  * The same checks as fa_bwd run first; an unknown stage is
  * FA_ERR_UNSUPPORTED.
  */
@@ -136,9 +156,10 @@ typedef enum { FA_BWD_PREPROCESS = 0, FA_BWD_DKDV = 1, FA_BWD_DQ_CONVERT = 2 } f
 fa_status fa_bwd_stage(int stage, const void* q, const void* k, const void* v, const void* o,
                        const void* dO, const float* lse, void* dq, void* dk, void* dv,
                        int B, int Hq, int Hkv, int N, int d, float scale, int causal,
-                       const int32_t* cu_seqlens, long long total_tokens,
+                       int window, const int32_t* cu_seqlens, long long total_tokens,
                        const float* alibi_slopes, fa_dtype dtype, fa_dtype o_dtype,
-                       void* workspace, size_t workspace_bytes, void* stream);
+                       int deterministic, void* workspace, size_t workspace_bytes,
+                       void* stream);
 
 /*
  * fa_bwd for callers that cannot allocate device memory.  (The pages have no
@@ -176,9 +197,9 @@ fa_status fa_bwd_stage(int stage, const void* q, const void* k, const void* v, c
 fa_status fa_bwd_static_scratch(const void* q, const void* k, const void* v, const void* o,
                                 const void* dO, const float* lse, void* dq, void* dk, void* dv,
                                 int B, int Hq, int Hkv, int N, int d, float scale, int causal,
-                                const int32_t* cu_seqlens, long long total_tokens,
+                                int window, const int32_t* cu_seqlens, long long total_tokens,
                                 const float* alibi_slopes, fa_dtype dtype, fa_dtype o_dtype,
-                                void* stream);
+                                int deterministic, void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status

@@ -63,7 +63,7 @@ def forward(x: I.Inputs, guard=True, check=True, out_dtype=None):
     lbuf, lse = guarded_empty((w.Hq, x.T), t.float32)
     fa.attention_forward(q, k, v, causal=w.causal, scale=x.scale, cu_seqlens=cu,
                          max_seqlen=w.N if w.varlen else None, batch=None if w.varlen else w.B,
-                         alibi_slopes=slopes, out=o, lse=lse, check=check)
+                         alibi_slopes=slopes, window=w.window, out=o, lse=lse, check=check)
     t.cuda.synchronize()
     if guard:
         assert_guards(obuf)
@@ -71,7 +71,7 @@ def forward(x: I.Inputs, guard=True, check=True, out_dtype=None):
     return as_f64(o), as_f64(lse)
 
 
-def backward(x: I.Inputs, guard=True, check=True, out_dtype=None):
+def backward(x: I.Inputs, guard=True, check=True, out_dtype=None, deterministic=False):
     """Run fa_fwd then fa_bwd; returns float64 numpy (O, LSE, dQ, dK, dV).
     O is stored as fp32 unless `out_dtype` says otherwise."""
     t = torch()
@@ -80,12 +80,12 @@ def backward(x: I.Inputs, guard=True, check=True, out_dtype=None):
     cu = t.from_numpy(x.cu_seqlens).cuda() if w.varlen else None
     slopes = t.from_numpy(x.alibi_slopes).cuda() if x.alibi_slopes is not None else None
     kw = dict(causal=w.causal, scale=x.scale, cu_seqlens=cu, max_seqlen=w.N if w.varlen else None,
-              batch=None if w.varlen else w.B, alibi_slopes=slopes, check=check)
+              batch=None if w.varlen else w.B, alibi_slopes=slopes, window=w.window, check=check)
     o, lse = fa.attention_forward(q, k, v, out_dtype=out_dtype or t.float32, **kw)
     bufs = [guarded_empty(q.shape, q.dtype), guarded_empty(k.shape, k.dtype),
             guarded_empty(v.shape, v.dtype)]
     dq, dk, dv = fa.attention_backward(q, k, v, o, do, lse, dq=bufs[0][1], dk=bufs[1][1],
-                                       dv=bufs[2][1], **kw)
+                                       dv=bufs[2][1], deterministic=deterministic, **kw)
     t.cuda.synchronize()
     if guard:
         for b, _ in bufs:

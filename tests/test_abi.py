@@ -48,21 +48,22 @@ A = 0x10000   # a fake, 256-byte aligned device address (never dereferenced)
 
 def fwd(**kw):
     a = dict(q=A, k=A, v=A, o=A, lse=A, B=1, Hq=2, Hkv=2, N=128, d=64, scale=0.125, causal=1,
-             cu=None, T=0, alibi=None, dtype=fa.FA_BF16, odt=fa.FA_BF16, stream=None)
+             window=-1, cu=None, T=0, alibi=None, dtype=fa.FA_BF16, odt=fa.FA_BF16, stream=None)
     a.update(kw)
     return fa.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["N"],
-                     a["d"], a["scale"], a["causal"], a["cu"], a["T"], a["alibi"], a["dtype"],
-                     a["odt"], a["stream"])
+                     a["d"], a["scale"], a["causal"], a["window"], a["cu"], a["T"], a["alibi"],
+                     a["dtype"], a["odt"], a["stream"])
 
 
 def bwd(**kw):
-    a = dict(B=1, Hq=2, Hkv=2, N=128, d=64, scale=0.125, causal=1, cu=None, T=0, alibi=None,
-             dtype=fa.FA_BF16, odt=fa.FA_FP32, ws=A, wsb=1 << 40, stream=None, ptr=A)
+    a = dict(B=1, Hq=2, Hkv=2, N=128, d=64, scale=0.125, causal=1, window=-1, cu=None, T=0,
+             alibi=None, dtype=fa.FA_BF16, odt=fa.FA_FP32, det=0, ws=A, wsb=1 << 40, stream=None,
+             ptr=A)
     a.update(kw)
     p = a["ptr"]
     return fa.fa_bwd(p, p, p, p, p, p, p, p, p, a["B"], a["Hq"], a["Hkv"], a["N"], a["d"],
-                     a["scale"], a["causal"], a["cu"], a["T"], a["alibi"], a["dtype"], a["odt"],
-                     a["ws"], a["wsb"], a["stream"])
+                     a["scale"], a["causal"], a["window"], a["cu"], a["T"], a["alibi"], a["dtype"],
+                     a["odt"], a["det"], a["ws"], a["wsb"], a["stream"])
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -75,6 +76,9 @@ def bwd(**kw):
     (dict(dtype=fa.FA_FP32, q=A + 2, odt=fa.FA_FP32), 4),
     (dict(dtype=fa.FA_FP32, odt=fa.FA_BF16), 3), (dict(odt=5), 3),
     (dict(B=0), 0), (dict(N=0), 0),        # empty: nothing to launch
+    (dict(window=4, causal=0), 3),         # a sliding window is a causal band
+    (dict(window=0, causal=0), 3),
+    (dict(window=4, B=0), 0), (dict(window=-7, causal=0, B=0), 0),
 ])
 def test_fwd_rejects_before_launch(lib, kw, code):
     assert fwd(**kw) == code
@@ -84,6 +88,8 @@ def test_fwd_rejects_before_launch(lib, kw, code):
     (dict(ptr=None), 1), (dict(Hq=4, Hkv=3), 2), (dict(odt=9), 3), (dict(d=32), 3), (dict(dtype=fa.FA_FP32), 3),
     (dict(ptr=A + 4), 4), (dict(ws=None), 5), (dict(wsb=1024), 5), (dict(ws=A + 16), 4),
     (dict(B=0), 0),
+    (dict(window=3, causal=0), 3), (dict(det=2), 3), (dict(det=-1), 3),
+    (dict(window=3, B=0), 0),
 ])
 def test_bwd_rejects_before_launch(lib, kw, code):
     assert bwd(**kw) == code
@@ -91,8 +97,8 @@ def test_bwd_rejects_before_launch(lib, kw, code):
 
 def test_bwd_stage_rejects_unknown_stage(lib):
     p = A
-    args = (p, p, p, p, p, p, p, p, p, 1, 2, 2, 128, 64, 0.125, 1, None, 0, None, fa.FA_BF16,
-            fa.FA_FP32, A, 1 << 40, None)
+    args = (p, p, p, p, p, p, p, p, p, 1, 2, 2, 128, 64, 0.125, 1, -1, None, 0, None, fa.FA_BF16,
+            fa.FA_FP32, 0, A, 1 << 40, None)
     assert fa.fa_bwd_stage(3, *args) == 3
     assert fa.fa_bwd_stage(-1, *args) == 3
     bad = list(args)

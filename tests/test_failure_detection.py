@@ -55,12 +55,13 @@ def test_malformed_cu_seqlens_reported(torch):
     o = torch.empty(q.shape, dtype=torch.float32, device="cuda")
     lse = torch.empty((2, x.T), dtype=torch.float32, device="cuda")
     st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), 3, 2, 2,
-                   64, 64, x.scale, 1, bad.data_ptr(), x.T, None, fa.FA_BF16, fa.FA_FP32, None)
+                   64, 64, x.scale, 1, -1, bad.data_ptr(), x.T, None, fa.FA_BF16, fa.FA_FP32, None)
     assert st == 0                                                   # detected on the device
     assert fa.fa_check_device_error(None) == 8                       # FA_ERR_CU_SEQLENS
     too_long = torch.tensor([0, 64, 192, 192], dtype=torch.int32, device="cuda")   # 128 > N=64
     st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), 3, 2, 2,
-                   64, 64, x.scale, 1, too_long.data_ptr(), x.T, None, fa.FA_BF16, fa.FA_FP32, None)
+                   64, 64, x.scale, 1, -1, too_long.data_ptr(), x.T, None, fa.FA_BF16, fa.FA_FP32,
+                   None)
     assert st == 0
     assert fa.fa_check_device_error(None) == 8
     _small_forward_ok(torch)

@@ -37,3 +37,14 @@ def test_inputs_are_bf16_exact_and_seeded():
 def test_attended_pairs():
     assert I.attended_pairs(I.workload("c3_long")) == 32 * 16384 * 16385 // 2
     assert I.attended_pairs(I.workload("c1_fp32_fwd")) == 128 * 128
+
+
+def test_attended_pairs_counts_the_band():
+    """Band area against a brute-force count of visible (i, j) pairs."""
+    for L, wnd in ((1, 0), (5, 0), (300, 40), (129, 128), (129, 127), (64, 1000)):
+        w = I.small_case("bf16", causal=True, B=1, Hq=3, Hkv=1, N=L, d=64, window=wnd)
+        brute = sum(1 for i in range(L) for j in range(L) if i - wnd <= j <= i)
+        assert I.attended_pairs(w) == 3 * brute
+    w = I.small_case("bf16", causal=True, Hq=2, Hkv=2, d=64, seqlens=(7, 0, 50), window=3)
+    brute = sum(1 for L in (7, 0, 50) for i in range(L) for j in range(L) if i - 3 <= j <= i)
+    assert I.attended_pairs(w) == 2 * brute

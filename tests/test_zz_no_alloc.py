@@ -33,8 +33,8 @@ def test_refuses_problems_larger_than_the_scratch(lib):
     A = 0x10000
     B, Hq, N, d = 1, 32, 16384, 128
     assert fa.fa_bwd_workspace_size(B, Hq, N, d, 0) > fa.FA_BWD_STATIC_SCRATCH_BYTES
-    st = fa.fa_bwd_static_scratch(A, A, A, A, A, A, A, A, A, B, Hq, Hq, N, d, 0.088, 1, None, 0,
-                                  None, fa.FA_BF16, fa.FA_FP32, None)
+    st = fa.fa_bwd_static_scratch(A, A, A, A, A, A, A, A, A, B, Hq, Hq, N, d, 0.088, 1, -1, None,
+                                  0, None, fa.FA_BF16, fa.FA_FP32, 0, None)
     assert st == 5
 
 
@@ -52,17 +52,18 @@ def _run_pair(w, seed):
     lse = torch.empty((w.Hq, T), dtype=torch.float32, device="cuda")
     sp = torch.cuda.current_stream().cuda_stream
     P = lambda t: None if t is None else t.data_ptr()
-    common = (w.B, w.Hq, w.Hkv, w.N, w.d, float(x.scale), int(w.causal), P(cu), T, P(slopes))
+    common = (w.B, w.Hq, w.Hkv, w.N, w.d, float(x.scale), int(w.causal), w.window_arg, P(cu), T,
+              P(slopes))
     assert fa.fa_fwd(P(q), P(k), P(v), P(o), P(lse), *common, fa.FA_BF16, fa.FA_FP32, sp) == 0
     ref = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
     ws_bytes = fa.fa_bwd_workspace_size(w.B, w.Hq, w.N, w.d, T)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     assert fa.fa_bwd(P(q), P(k), P(v), P(o), P(do), P(lse), *(P(t) for t in ref), *common,
-                     fa.FA_BF16, fa.FA_FP32, P(ws), ws_bytes, sp) == 0
+                     fa.FA_BF16, fa.FA_FP32, 0, P(ws), ws_bytes, sp) == 0
     got = [torch.full_like(q, float("nan")), torch.full_like(k, float("nan")),
            torch.full_like(v, float("nan"))]
     assert fa.fa_bwd_static_scratch(P(q), P(k), P(v), P(o), P(do), P(lse), *(P(t) for t in got),
-                                    *common, fa.FA_BF16, fa.FA_FP32, sp) == 0
+                                    *common, fa.FA_BF16, fa.FA_FP32, 0, sp) == 0
     assert fa.fa_check_device_error(sp) == 0
     f64 = lambda t: t.double().cpu().numpy()
     return [f64(t) for t in ref], [f64(t) for t in got]
