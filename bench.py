@@ -55,6 +55,8 @@ def parse():
                     choices=sorted(I.WORKLOADS) + sorted(I.EXTRA_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="time the deterministic backward (dQ by its own kernel, no atomics)")
     return ap.parse_args()
 
 
@@ -224,7 +226,8 @@ def run_ours(args, world, rank, local):
     common = (w.B, w.Hq, w.Hkv, w.N, w.d, float(x.scale), int(w.causal), w.window_arg, P(cu), T,
               P(slopes))
     ptrs = (P(q), P(k), P(v), P(o), P(do), P(lse), P(dq), P(dk), P(dv))
-    names = ["fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq_convert"]
+    det = 1 if args.deterministic else 0
+    names = ["fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq" if det else "bwd_dq_convert"]
 
     def step(evs=None):
         if evs is not None:
@@ -240,7 +243,7 @@ def run_ours(args, world, rank, local):
         for s in range(3):
             if evs is not None:
                 evs[1 + s].record(stream)
-            st = fa.fa_bwd_stage(s, *ptrs, *common, fa.FA_BF16, fa.FA_FP32, 0, P(ws), ws_bytes,
+            st = fa.fa_bwd_stage(s, *ptrs, *common, fa.FA_BF16, fa.FA_FP32, det, P(ws), ws_bytes,
                                  sp)
             if st:
                 raise fa.FAError(st, "fa_bwd_stage")
@@ -290,7 +293,14 @@ def run_ours(args, world, rank, local):
     kern_ms = {}
     for j, name in enumerate(names[:nev - 1]):
         kern_ms[name] = statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evsets)
-    kern_flops = {"fwd": fl["fwd"], "bwd_dkdv": fl["bwd"]}
+    # FLOPs each kernel's MMAs must do: the default dK/dV kernel runs all
+    # five backward products (10 d per pair); in the deterministic backward it
+    # runs four (S, dP, dV, dK: 8 d) and the dQ kernel three (S, dP, dQ: 6 d).
+    if det:
+        kern_flops = {"fwd": fl["fwd"], "bwd_dkdv": 8.0 * w.d * fl["pairs"],
+                      "bwd_dq": 6.0 * w.d * fl["pairs"]}
+    else:
+        kern_flops = {"fwd": fl["fwd"], "bwd_dkdv": fl["bwd"]}
     dom = max(kern_ms, key=lambda n: kern_ms[n])
     peak, hbm, peak_src = load_peaks()
     if dom in kern_flops:
@@ -298,10 +308,10 @@ def run_ours(args, world, rank, local):
         roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(ach / peak, 4),
                 "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
-                "traffic": ncu_traffic(w.name, dom)}
+                "traffic": ncu_traffic(w.name + (" deterministic" if det else ""), dom)}
     else:
         roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s",
-                "frac": None, "traffic": ncu_traffic(w.name, dom)}
+                "frac": None, "traffic": ncu_traffic(w.name + (" deterministic" if det else ""), dom)}
     per_kernel = {n: {"ms": round(kern_ms[n], 4),
                       "tflops": round(kern_flops[n] / (kern_ms[n] * 1e-3) / 1e12, 1)
                       if n in kern_flops else None,
@@ -326,6 +336,7 @@ def run_ours(args, world, rank, local):
         "data": "synthetic (seeded PCG64, seed 0; no dataset)",
         "config": {"workload": w.name, "desc": w.note, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
                    "N": w.N, "d": w.d, "causal": w.causal, "window": w.window,
+                   "deterministic_bwd": bool(det),
                    "alibi": w.alibi, "varlen": w.varlen,
                    "total_tokens": T, "o_dtype": "fp32", "flops_per_step": fl["total"],
                    "pct_of_peak": round(100.0 * value / world / peak, 2),

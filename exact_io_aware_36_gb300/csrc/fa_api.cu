@@ -156,7 +156,6 @@ static fa_status bwd_impl(int stage, const void* q, const void* k, const void* v
   if (o_dtype != FA_FP32 && o_dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
   if (window >= 0 && !causal) return FA_ERR_UNSUPPORTED;
   if (deterministic != 0 && deterministic != 1) return FA_ERR_UNSUPPORTED;
-  if (deterministic) return FA_ERR_UNSUPPORTED;
   if (stage < -1 || stage > 2) return FA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||

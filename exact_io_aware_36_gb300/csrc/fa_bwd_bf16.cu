@@ -98,23 +98,10 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-__device__ __forceinline__ bool seq_bounds(const AttnParams& p, int b, long long* seq0, int* L) {
-  if (p.cu_seqlens) {
-    const int c0 = __ldg(p.cu_seqlens + b);
-    const int c1 = __ldg(p.cu_seqlens + b + 1);
-    if ((b == 0 && c0 != 0) || c1 < c0 || (long long)c1 > p.T || c1 - c0 > p.N) return false;
-    *seq0 = c0;
-    *L = c1 - c0;
-  } else {
-    *seq0 = (long long)b * p.N;
-    *L = p.N;
-  }
-  return true;
-}
-
 // ----------------------------------------------------------------- preprocess
 // One warp per (token, query head): D = dO . O in fp32, and the dQ
-// accumulator row zeroed.
+// accumulator row zeroed (not in the deterministic backward, which has no
+// accumulator).
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const AttnParams p) {
   const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -149,6 +136,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const AttnParams p)
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
   if (lane == 0) p.D[(long long)h * p.T + t] = acc;
+  if (p.deterministic) return;           // dQ has its own kernel: no accumulator
   float4* z = reinterpret_cast<float4*>(p.dq_acc + ((long long)h * p.T + t) * D);
   if (lane < D / 4) z[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
@@ -176,7 +164,9 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const AttnParams p)
 
 // ---------------------------------------------------------------------- dkdv
 // BAND: causal band (sliding window p.window); only with CAUSAL.
-template <int D, bool CAUSAL, bool ALIBI, bool BAND>
+// DQ: also accumulate dQ into the workspace (otherwise the deterministic
+// backward's dQ kernel computes it; this kernel then writes dK and dV only).
+template <int D, bool CAUSAL, bool ALIBI, bool BAND, bool DQ>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -370,28 +360,32 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mma_commit(&bars->q_empty[st]);
       }
       __syncwarp();
-      // dq_full(it) must not complete before the drain has seen dq_full(it-1)
-      // (a skipped phase would leave the drain waiting for good).  Steps
-      // it-1 < n-2 already waited for that drain before dP(it+1); the last
-      // step did not, so it waits here.
-      if (it >= 1 && it + 1 >= n_iter && !(ok = wait_warp(&bars->dq_free, (it - 1) & 1, wc))) break;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t dsb = sdS + buf * C::DS_BYTES;
+      if (DQ) {
+        // dq_full(it) must not complete before the drain has seen dq_full(it-1)
+        // (a skipped phase would leave the drain waiting for good).  Steps
+        // it-1 < n-2 already waited for that drain before dP(it+1); the last
+        // step did not, so it waits here.
+        if (it >= 1 && it + 1 >= n_iter && !(ok = wait_warp(&bars->dq_free, (it - 1) & 1, wc))) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t dsb = sdS + buf * C::DS_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)   // dQ^T = K^T dS^T   (K = 128 keys)
-          mma_ss(tmem + C::PB_COL0 + 64 * buf, smem_desc_sw128(sK + kk * 2048, C::KV_BOX, 1024),
-                 smem_desc_sw128(dsb + kk * 2048, C::Q_BOX, 1024), ID_DQ, kk > 0 ? 1u : 0u);
-        mma_commit(&bars->dq_full);
+          for (int kk = 0; kk < 8; ++kk)   // dQ^T = K^T dS^T   (K = 128 keys)
+            mma_ss(tmem + C::PB_COL0 + 64 * buf, smem_desc_sw128(sK + kk * 2048, C::KV_BOX, 1024),
+                   smem_desc_sw128(dsb + kk * 2048, C::Q_BOX, 1024), ID_DQ, kk > 0 ? 1u : 0u);
+          mma_commit(&bars->dq_full);
+        }
+        __syncwarp();
       }
-      __syncwarp();
       const int nx = it + 2;
       if (nx < n_iter) {
         if (!(ok = wait_warp(&bars->q_full[nx % kQStages], (nx / kQStages) & 1, wc))) break;
         tc_fence_after();
         if (lane == 0) issue_s(nx);
         __syncwarp();
-        if (!(ok = wait_warp(&bars->dq_free, it & 1, wc))) break;
+        // dP(nx) reuses the columns of dQ^T(it) (DQ) or of dS^T(it), which
+        // the dK(it) MMA issued above reads first (MMAs run in issue order)
+        if (DQ && !(ok = wait_warp(&bars->dq_free, it & 1, wc))) break;
         tc_fence_after();
         if (lane == 0) {
           issue_dp(nx);
@@ -467,15 +461,17 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         tmem_st16(tSb + 16 * half, pk);          // P^T (bf16) over consumed S^T columns
         tmem_st16(tPb + 16 * half, dk);          // dS^T (bf16) over consumed dP^T columns
+        if (DQ) {
 #pragma unroll
-        for (int q16 = 0; q16 < 4; ++q16) {      // dS^T row into shared memory (swizzled)
-          const int chunk = 4 * half + q16;
-          const int phys = chunk ^ (kr & 7);
-          *reinterpret_cast<uint4*>(dsrow + phys * 16) =
-              make_uint4(dk[4 * q16], dk[4 * q16 + 1], dk[4 * q16 + 2], dk[4 * q16 + 3]);
+          for (int q16 = 0; q16 < 4; ++q16) {    // dS^T row into shared memory (swizzled)
+            const int chunk = 4 * half + q16;
+            const int phys = chunk ^ (kr & 7);
+            *reinterpret_cast<uint4*>(dsrow + phys * 16) =
+                make_uint4(dk[4 * q16], dk[4 * q16 + 1], dk[4 * q16 + 2], dk[4 * q16 + 3]);
+          }
         }
       }
-      fence_proxy_async_smem();
+      if (DQ) fence_proxy_async_smem();
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -509,7 +505,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const uint32_t lane_base = tmem + ((uint32_t)(32 * q4) << 16);
     float* dqs = reinterpret_cast<float*>(smem + C::DQ_OFF);
     bool ok = true;
-    for (int it = 0; it < n_iter; ++it) {
+    for (int it = 0; DQ && it < n_iter; ++it) {
       const int buf = it & 1;
       const int h = g * p.group + it / nqt;
       const int q0 = (qt0 + it % nqt) * 64;
@@ -545,7 +541,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         __syncwarp();
       }
     }
-    if (q4 == 0 && lane == 0) bulk_wait_group0();
+    if (DQ && q4 == 0 && lane == 0) bulk_wait_group0();
     __syncwarp();
     // dK epilogue
     if (ok) ok = wait_warp(&bars->dkdv_done, 0, wc);
@@ -582,10 +578,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   }
 }
 
-template <int D, bool CAUSAL, bool ALIBI, bool BAND>
+template <int D, bool CAUSAL, bool ALIBI, bool BAND, bool DQ>
 int launch_dkdv(const AttnParams& p, cudaStream_t stream) {
   using C = BwdCfg<D>;
-  auto kern = bwd_dkdv_kernel<D, CAUSAL, ALIBI, BAND>;
+  auto kern = bwd_dkdv_kernel<D, CAUSAL, ALIBI, BAND, DQ>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return (int)e;
   CUtensorMap tq, tk, tv, tdo;
@@ -599,6 +595,16 @@ int launch_dkdv(const AttnParams& p, cudaStream_t stream) {
   return (int)cudaGetLastError();
 }
 
+template <int D, bool DQ>
+int launch_dkdv_masks(const AttnParams& p, cudaStream_t stream) {
+  const bool alibi = p.alibi != nullptr;
+  if (p.causal && p.window != kNoWindow)
+    return alibi ? launch_dkdv<D, true, true, true, DQ>(p, stream) : launch_dkdv<D, true, false, true, DQ>(p, stream);
+  if (p.causal)
+    return alibi ? launch_dkdv<D, true, true, false, DQ>(p, stream) : launch_dkdv<D, true, false, false, DQ>(p, stream);
+  return alibi ? launch_dkdv<D, false, true, false, DQ>(p, stream) : launch_dkdv<D, false, false, false, DQ>(p, stream);
+}
+
 template <int D>
 int launch_stages(const AttnParams& p, cudaStream_t stream, int stage) {
   const long long rows = p.T * p.Hq;
@@ -608,17 +614,12 @@ int launch_stages(const AttnParams& p, cudaStream_t stream, int stage) {
     if (e != cudaSuccess) return (int)e;
   }
   if (stage < 0 || stage == 1) {
-    int r;
-    const bool alibi = p.alibi != nullptr;
-    if (p.causal && p.window != kNoWindow)
-      r = alibi ? launch_dkdv<D, true, true, true>(p, stream) : launch_dkdv<D, true, false, true>(p, stream);
-    else if (p.causal)
-      r = alibi ? launch_dkdv<D, true, true, false>(p, stream) : launch_dkdv<D, true, false, false>(p, stream);
-    else
-      r = alibi ? launch_dkdv<D, false, true, false>(p, stream) : launch_dkdv<D, false, false, false>(p, stream);
+    const int r = p.deterministic ? launch_dkdv_masks<D, false>(p, stream)
+                                  : launch_dkdv_masks<D, true>(p, stream);
     if (r) return r;
   }
   if (stage < 0 || stage == 2) {
+    if (p.deterministic) return launch_bwd_dq_bf16(p, stream);
     const long long n8 = rows * (D / 8);
     bwd_dq_convert_kernel<D><<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(p);
     return (int)cudaGetLastError();

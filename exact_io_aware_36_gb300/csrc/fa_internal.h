@@ -50,6 +50,25 @@ struct AttnParams {
 int launch_fwd_fp32(const AttnParams& p, void* stream);
 int launch_fwd_bf16(const AttnParams& p, void* stream);
 int launch_bwd_bf16(const AttnParams& p, void* stream, int stage);   // stage < 0: all
+int launch_bwd_dq_bf16(const AttnParams& p, void* stream);            // deterministic dQ
 int launch_selftest_wait(unsigned int* status, unsigned long long limit_ns, void* stream);
+
+#ifdef __CUDACC__
+// Start token and length of sequence b; false when cu_seqlens is malformed
+// there or the sequence is longer than N.
+__device__ __forceinline__ bool seq_bounds(const AttnParams& p, int b, long long* seq0, int* L) {
+  if (p.cu_seqlens) {
+    const int c0 = __ldg(p.cu_seqlens + b);
+    const int c1 = __ldg(p.cu_seqlens + b + 1);
+    if ((b == 0 && c0 != 0) || c1 < c0 || (long long)c1 > p.T || c1 - c0 > p.N) return false;
+    *seq0 = c0;
+    *L = c1 - c0;
+  } else {
+    *seq0 = (long long)b * p.N;
+    *L = p.N;
+  }
+  return true;
+}
+#endif
 
 }  // namespace fa
