@@ -363,9 +363,11 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       // due and the pass is exactly what the full path would produce.
       float ts = 0.f, tsr = 0.f;
       bool full = __any_sync(0xffffffffu, m_ref == -INFINITY);
+      bool spec_over = false;     // this row's speculative sum exceeded 2^tau
       if (!full) {
         exp_pass(m_ref, ts, tsr);
-        full = __any_sync(0xffffffffu, !(ts <= kSpecSum));   // also catches inf / nan
+        spec_over = !(ts <= kSpecSum);                      // also catches inf / nan
+        full = __any_sync(0xffffffffu, spec_over);
         if (full) tmem_wait_st();
       }
       if (full) {
@@ -390,8 +392,13 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         float xmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
         if (!ALIBI) xmax *= c2;
-        // lazy rescale: raise the reference only when the max grew past tau
-        const bool raise = xmax > m_ref + kTau;
+        // Lazy rescale: raise the reference when the max grew past tau, and
+        // also when this row's speculative sum overflowed (its max then
+        // exceeds the reference; without the raise every later tile of a
+        // row whose reference came from a few keys would fail the
+        // speculation again).  Either choice of reference gives the same
+        // result.
+        const bool raise = xmax > m_ref + kTau || spec_over;
         const float m_new = raise ? xmax : m_ref;
         const float alpha = raise ? ex2_approx(m_ref - m_new) : 1.f;
         l *= alpha;
