@@ -44,6 +44,13 @@ R8  No dropout (the usage contract's example passes dropout_p = 0.0).
 R9  Sliding window (named only, among the mask variants of the usage contract
     table): a causal band, key j visible to query i iff i - window <= j <= i;
     window None (or < 0) means no window; window requires causal.
+R10 Decode over a KV cache (named only: flash_attn_with_kvcache and the
+    small-query paths in [FA1 note] "Long context and inference remain
+    unsolved"): sequence b holds L_b cached tokens, the new ones included; its
+    q_len query rows are its newest tokens, at positions L_b - q_len + i, and
+    attend under R6 (causal, positions local to the sequence), with R4's bias
+    and R9's window.  Decode therefore equals the last q_len rows of the
+    causal forward over the whole sequence.
 """
 from __future__ import annotations
 
@@ -53,6 +60,7 @@ __all__ = [
     "attention_forward", "attention_backward", "head_forward", "head_backward",
     "head_scores", "online_softmax_forward", "online_softmax_forward_normalised",
     "forward_rows", "backward_query_rows", "backward_key_rows", "head_row_stats",
+    "decode_forward",
 ]
 
 
@@ -444,3 +452,48 @@ def backward_key_rows(q, k, v, do, scale, causal, rows, cu_seqlens=None,
         outK.append(dk)
         outV.append(dv)
     return np.array(outK), np.array(outV)
+
+
+# --------------------------------------------------------------------------
+# Decode: the newest tokens of each sequence against its KV cache (R10).
+# --------------------------------------------------------------------------
+
+def decode_forward(q, k_cache, v_cache, cache_seqlens, scale, q_len=1, alibi_slopes=None,
+                   window=None):
+    """O and LSE of the q_len newest tokens of every sequence (R10).
+
+    q: [B * q_len, Hq, d], rows b * q_len .. b * q_len + q_len - 1 belonging to
+    sequence b; k_cache, v_cache: [B, S_max, Hkv, d]; cache_seqlens: [B] (None:
+    every sequence holds S_max tokens).  Row i of sequence b is the query at
+    position p_i = L_b - q_len + i; keys j < L_b of its cache; S = scale q k^T
+    plus R4's bias -slope (p_i - j), masked where j > p_i or (R9)
+    j < p_i - window; P = softmax(S) ([FA1 note] Key design 1); O = P V.
+    Returns O [B * q_len, Hq, d] and LSE [Hq, B * q_len].
+    """
+    B, S_max, Hkv, d = k_cache.shape
+    Hq = q.shape[1]
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    group = Hq // Hkv
+    window = _window(window, True)
+    O = np.empty((B * q_len, Hq, v_cache.shape[3]))
+    LSE = np.empty((Hq, B * q_len))
+    for b in range(B):
+        L = S_max if cache_seqlens is None else int(cache_seqlens[b])
+        if not q_len <= L <= S_max:
+            raise ValueError("a cache must hold its q_len new tokens and at most S_max")
+        pos = (L - q_len + np.arange(q_len))[:, None]
+        j = np.arange(L)[None, :]
+        vis = j <= pos
+        if window is not None:
+            vis &= j >= pos - window
+        rows = slice(b * q_len, (b + 1) * q_len)
+        for h in range(Hq):
+            g = h // group
+            S = scale * (_f64(q[rows, h]) @ _f64(k_cache[b, :L, g]).T)
+            if alibi_slopes is not None:
+                S = S - float(alibi_slopes[h]) * (pos - j)
+            P, lse = _softmax_rows(np.where(vis, S, -np.inf))
+            O[rows, h] = P @ _f64(v_cache[b, :L, g])
+            LSE[h, rows] = lse
+    return O, LSE

@@ -424,3 +424,84 @@ def test_window_sampled_rows_equal_full_oracle():
     for n, (t, g) in enumerate(krows):
         np.testing.assert_allclose(dk_r[n], dk[t, g], atol=1e-12)
         np.testing.assert_allclose(dv_r[n], dv[t, g], atol=1e-12)
+
+
+# ------------------------------------------------------------------- decode
+
+def _cache_case(seed, lens, S_max, Hq, Hkv, d, q_len):
+    """Sequences of the given lengths laid out as a [B, S_max, Hkv, d] cache
+    (slots past each length hold garbage), with the newest q_len tokens' queries."""
+    B = len(lens)
+    kc = rnd(seed, B, S_max, Hkv, d)
+    vc = rnd(seed + 1, B, S_max, Hkv, d)
+    qf = rnd(seed + 2, B, S_max, Hq, d)          # queries of every position
+    q = np.concatenate([qf[b, L - q_len:L] for b, L in enumerate(lens)])
+    return q, kc, vc, qf
+
+
+@pytest.mark.parametrize("q_len,alibi,window,Hq,Hkv", [
+    (1, False, None, 4, 2), (1, True, None, 8, 2), (3, False, None, 2, 2),
+    (4, True, 5, 4, 1), (1, False, 0, 2, 1), (2, False, 40, 3, 3)])
+def test_decode_is_the_last_rows_of_the_causal_forward(q_len, alibi, window, Hq, Hkv):
+    """R10: decode equals the causal forward over each whole sequence, read at
+    its newest q_len rows (the forward is pinned by the tests above)."""
+    lens, S_max, d, scale = [37, 4, 60], 64, 8, 0.3
+    q, kc, vc, qf = _cache_case(70, lens, S_max, Hq, Hkv, d, q_len)
+    slopes = I.alibi_slopes(Hq).astype(np.float64) if alibi else None
+    O, lse = A.decode_forward(q, kc, vc, np.array(lens), scale, q_len, slopes, window)
+    for b, L in enumerate(lens):
+        Of, lf = A.attention_forward(qf[b, :L], kc[b, :L], vc[b, :L], scale, True, None, slopes,
+                                     window=window)
+        np.testing.assert_allclose(O[b * q_len:(b + 1) * q_len], Of[L - q_len:], atol=1e-12)
+        np.testing.assert_allclose(lse[:, b * q_len:(b + 1) * q_len], lf[:, L - q_len:], atol=1e-12)
+
+
+@pytest.mark.parametrize("window", [None, 0, 3])
+def test_decode_equal_keys_give_the_visible_mean(window):
+    """With all keys zero every visible score is 0 (no bias): O is the mean of
+    the visible values and LSE = log(count)."""
+    lens, S_max, Hq, Hkv, d, q_len = [9, 2, 16], 16, 2, 1, 4, 2
+    q, kc, vc, _ = _cache_case(80, lens, S_max, Hq, Hkv, d, q_len)
+    kc[:] = 0.0
+    O, lse = A.decode_forward(q, kc, vc, np.array(lens), 0.5, q_len, None, window)
+    for b, L in enumerate(lens):
+        for i in range(q_len):
+            p = L - q_len + i
+            lo = 0 if window is None else max(0, p - window)
+            for h in range(Hq):
+                np.testing.assert_allclose(O[b * q_len + i, h], vc[b, lo:p + 1, 0].mean(0), atol=1e-13)
+                assert abs(lse[h, b * q_len + i] - math.log(p + 1 - lo)) < 1e-13
+
+
+def test_decode_single_cached_token():
+    """L = 1: the one key is the answer; LSE = scale q . k."""
+    q, kc, vc, _ = _cache_case(90, [1, 1], 4, 2, 2, 8, 1)
+    O, lse = A.decode_forward(q, kc, vc, np.array([1, 1]), 0.7, 1)
+    for b in range(2):
+        for h in range(2):
+            np.testing.assert_allclose(O[b, h], vc[b, 0, h], atol=1e-14)
+            assert abs(lse[h, b] - 0.7 * q[b, h] @ kc[b, 0, h]) < 1e-13
+
+
+def test_decode_matches_torch_float64_sdpa():
+    torch = pytest.importorskip("torch")
+    lens, S_max, Hq, Hkv, d, q_len, scale = [50, 7], 64, 4, 2, 16, 3, 0.25
+    q, kc, vc, _ = _cache_case(95, lens, S_max, Hq, Hkv, d, q_len)
+    slopes = I.alibi_slopes(Hq).astype(np.float64)
+    O, lse = A.decode_forward(q, kc, vc, np.array(lens), scale, q_len, slopes, 20)
+    g = Hq // Hkv
+    for b, L in enumerate(lens):
+        tq = torch.tensor(q[b * q_len:(b + 1) * q_len].transpose(1, 0, 2)[None])
+        tk = torch.tensor(np.repeat(kc[b, :L], g, 1).transpose(1, 0, 2)[None])
+        tv = torch.tensor(np.repeat(vc[b, :L], g, 1).transpose(1, 0, 2)[None])
+        i = torch.arange(L - q_len, L, dtype=torch.float64)[:, None]
+        j = torch.arange(L, dtype=torch.float64)[None, :]
+        mask = torch.tensor(slopes)[:, None, None] * (j - i)[None]
+        mask = mask.masked_fill(((j > i) | (j < i - 20))[None], float("-inf"))
+        out = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask[None],
+                                                               scale=scale)
+        np.testing.assert_allclose(O[b * q_len:(b + 1) * q_len],
+                                   out[0].numpy().transpose(1, 0, 2), atol=1e-12)
+        scores = torch.einsum("hid,hjd->hij", tq[0], tk[0]) * scale + mask
+        np.testing.assert_allclose(lse[:, b * q_len:(b + 1) * q_len],
+                                   torch.logsumexp(scores, -1).numpy(), atol=1e-12)

@@ -140,3 +140,68 @@ def test_gqa_mapping_mistake_is_caught(monkeypatch):
     with pytest.raises(AssertionError):
         P.test_gqa_equals_mha_with_repeated_kv()
     assert orig_fwd is A.attention_forward
+
+
+# ------------------------------------------------------------------- decode
+
+_orig_decode = A.decode_forward
+
+
+def _decode_mutant(kind):
+    """decode_forward with one plausible mistake, written out in full."""
+    def f(q, k_cache, v_cache, cache_seqlens, scale, q_len=1, alibi_slopes=None, window=None):
+        B, S_max, Hkv, d = k_cache.shape
+        Hq = q.shape[1]
+        group = Hq // Hkv
+        O = np.empty((B * q_len, Hq, v_cache.shape[3]))
+        LSE = np.empty((Hq, B * q_len))
+        for b in range(B):
+            L = S_max if cache_seqlens is None else int(cache_seqlens[b])
+            off = L - q_len + (1 if kind == "position_plus_one" else 0)
+            pos = (off + np.arange(q_len))[:, None]
+            j = np.arange(L)[None, :]
+            vis = j <= pos
+            if window is not None:
+                vis &= j > pos - window if kind == "window_strict" else j >= pos - window
+            rows = slice(b * q_len, (b + 1) * q_len)
+            for h in range(Hq):
+                g = h % Hkv if kind == "kv_head_interleaved" else h // group
+                S = scale * (np.asarray(q[rows, h], np.float64) @ np.asarray(k_cache[b, :L, g], np.float64).T)
+                if alibi_slopes is not None:
+                    sgn = -1.0 if kind == "alibi_sign" else 1.0
+                    S = S - sgn * float(alibi_slopes[h]) * (pos - j)
+                P_, lse = A._softmax_rows(np.where(vis, S, -np.inf))
+                O[rows, h] = P_ @ np.asarray(v_cache[b, :L, g], np.float64)
+                LSE[h, rows] = lse
+        return O, LSE
+    return f
+
+
+DECODE_PINS = [
+    lambda: P.test_decode_is_the_last_rows_of_the_causal_forward(3, False, None, 2, 2),
+    lambda: P.test_decode_is_the_last_rows_of_the_causal_forward(1, True, None, 8, 2),
+    lambda: P.test_decode_is_the_last_rows_of_the_causal_forward(4, True, 5, 4, 1),
+    lambda: P.test_decode_equal_keys_give_the_visible_mean(3),
+    P.test_decode_matches_torch_float64_sdpa,
+]
+
+
+@pytest.mark.parametrize("kind", ["position_plus_one", "window_strict", "kv_head_interleaved",
+                                  "alibi_sign"])
+def test_planted_decode_mistake_is_caught(kind, monkeypatch):
+    monkeypatch.setattr(A, "decode_forward", _decode_mutant(kind))
+    caught = 0
+    for pin in DECODE_PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            caught += 1
+    assert caught, f"no pin catches decode mutant {kind}"
+
+
+def test_decode_mutant_harness_passes_unmutated(monkeypatch):
+    """The written-out copy without a mistake passes every decode pin, so the
+    failures above come from the planted mistakes."""
+    monkeypatch.setattr(A, "decode_forward", _decode_mutant("none"))
+    for pin in DECODE_PINS:
+        pin()
