@@ -33,6 +33,8 @@ import sys
 import tempfile
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -52,7 +54,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="c3_long",
-                    choices=sorted(I.WORKLOADS) + sorted(I.EXTRA_WORKLOADS))
+                    choices=sorted(I.WORKLOADS) + sorted(I.EXTRA_WORKLOADS) +
+                    sorted(I.DECODE_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--deterministic", action="store_true",
@@ -193,6 +196,153 @@ def smi_index(local: int) -> int:
     if local < len(parts) and parts[local].strip().isdigit():
         return int(parts[local])
     return local
+
+
+# ------------------------------------------------------------------ decode
+
+DECODE_METRIC = "decode attention over a KV cache: HBM bytes moved per second"
+
+
+def oracle_decode_sample(w, x):
+    """All query rows of one sequence (sequence 0) of a decode step through the
+    oracle as it stands; returns (bytes that step moves for it, seconds, what)."""
+    from oracle import attention_fp64 as A
+    t0 = time.perf_counter()
+    A.decode_forward(x.q[:w.q_len], x.cache("k", [0]), x.cache("v", [0]), x.seqlens[:1], x.scale,
+                     w.q_len, x.alibi_slopes, w.window)
+    dt = time.perf_counter() - t0
+    nbytes = I.decode_bytes(dataclasses.replace(w, B=1), x.seqlens[:1])
+    return nbytes, dt, f"sequence 0 of {w.B} (cache of {int(x.seqlens[0])} tokens), all {w.Hq} heads"
+
+
+def run_decode(args, world, rank, local):
+    """One step = one fa_decode call (split + combine kernels) over the whole
+    batch; `value` = the HBM bytes the step must move (every cached key and
+    value once, q, O, LSE) per second."""
+    import torch
+    from exact_io_aware_36_gb300 import fa
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = I.DECODE_WORKLOADS[args.workload]
+    x = I.make_decode_inputs(w, seed=0)
+    nbytes = I.decode_bytes(w, x.seqlens)
+
+    def todev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q, kc, vc = todev(x.q_bits), todev(x.k_bits), todev(x.v_bits)
+    cs = torch.from_numpy(x.seqlens.astype(np.int32)).to(dev)
+    slopes = torch.from_numpy(x.alibi_slopes).to(dev) if w.alibi else None
+    o = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    lse = torch.empty((w.Hq, q.shape[0]), dtype=torch.float32, device=dev)
+    ws_bytes = fa.fa_decode_workspace_size(w.B, w.Hq, w.Hkv, w.S_max, w.q_len, w.d)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    P = lambda t: None if t is None else t.data_ptr()
+
+    def step():
+        st = fa.fa_decode(P(q), P(kc), P(vc), P(cs), P(o), P(lse), w.B, w.Hq, w.Hkv, w.S_max,
+                          w.q_len, w.d, float(x.scale), w.window_arg, P(slopes), fa.FA_FP32,
+                          P(ws), ws_bytes, sp)
+        if st:
+            raise fa.FAError(st, "fa_decode")
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize(dev)
+    st = fa.fa_check_device_error(sp)
+    if st:
+        raise fa.FAError(st, "warm-up")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(smi_index(local))
+    sampler.start()
+    time.sleep(0.1)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    st = fa.fa_check_device_error(sp)
+    if st:
+        raise fa.FAError(st, "timed region")
+    total_ms = max_over_ranks(start.elapsed_time(end), world, dev)
+    ms_step = total_ms / args.steps
+    gbs = world * nbytes / (ms_step * 1e-3) / 1e9
+    call_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    _, hbm, src = load_peaks()
+    ach = nbytes / (call_ms * 1e-3) / 1e9
+    roof = {"kernel": "decode_split + decode_combine (one fa_decode call)", "bound": "hbm",
+            "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
+            "peak_source": f"{src} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+            "traffic": ncu_traffic(w.name, "decode")}
+    e2e = None
+    if not args.no_e2e:
+        hq = torch.from_numpy(np.ascontiguousarray(x.q_bits).view(np.int16)).view(torch.bfloat16).pin_memory()
+        hcs = torch.from_numpy(x.seqlens.astype(np.int32)).pin_memory()
+        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            cs.copy_(hcs, non_blocking=True)
+            step()
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / args.steps
+        e2e = {"value": round(world * nbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+               "ms_per_step": round(ms, 4),
+               "h2d_bytes_per_step": hq.numel() * 2 + hcs.numel() * 4,
+               "d2h_bytes_per_step": ho.numel() * 4 + hl.numel() * 4,
+               "path": "fa_decode through the C ABI; new tokens' q and cache lengths copied in, "
+                       "O and LSE copied out (the cache stays resident)"}
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cb, dt, what = oracle_decode_sample(w, x)
+        cpu = {"value": round(cb / dt / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
+               "kind": "oracle", "sample": what, "seconds": round(dt, 2),
+               "note": "NumPy float64; BLAS threads = all cores"}
+    line = {
+        "metric": DECODE_METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded PCG64, seed 0; no dataset)",
+        "config": {"workload": w.name, "desc": w.note, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "S_max": w.S_max, "d": w.d, "q_len": w.q_len,
+                   "cache_tokens": int(x.seqlens.sum()), "bytes_per_step": nbytes,
+                   "alibi": w.alibi, "window": w.window, "o_dtype": "fp32",
+                   "pct_of_hbm_peak": round(100.0 * gbs / world / hbm, 2),
+                   "l2": f"cache {nbytes / 1e9:.2f} GB read per step exceeds L2; no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
 
 
 # --------------------------------------------------------------------- ours
@@ -431,28 +581,36 @@ def cpu_baseline(w, x):
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    w = I.workload(args.workload)
-    x = I.make_inputs(w, seed=0)
+    if args.workload in I.DECODE_WORKLOADS:
+        w = I.DECODE_WORKLOADS[args.workload]
+        x = I.make_decode_inputs(w, seed=0)
+        sample_fn, metric, unit, scale = oracle_decode_sample, DECODE_METRIC, "GB/s", 1e9
+        shape = {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S_max": w.S_max, "d": w.d, "q_len": w.q_len,
+                 "step": "all query rows of one sequence of the decode step per step"}
+    else:
+        w = I.workload(args.workload)
+        x = I.make_inputs(w, seed=0)
+        sample_fn, metric, unit, scale = oracle_sample, METRIC, UNIT, 1e12
+        shape = {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal,
+                 "step": "one (sequence, head) sample of the workload per step"}
     for _ in range(max(args.warmup, 0)):
-        oracle_sample(w, x)
+        sample_fn(w, x)
     tot_fl, tot_dt, sample = 0.0, 0.0, ""
     for _ in range(args.steps):
-        fl, dt, sample = oracle_sample(w, x)
+        fl, dt, sample = sample_fn(w, x)
         tot_fl += fl
         tot_dt += dt
-    value = tot_fl / tot_dt / 1e12
+    value = tot_fl / tot_dt / scale
     line = {
-        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "metric": metric, "value": round(value, 6), "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * tot_dt / max(args.steps, 1), 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded PCG64, seed 0; no dataset)", "impl": "reference",
-        "config": {"workload": w.name, "desc": w.note, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
-                   "N": w.N, "d": w.d, "causal": w.causal,
-                   "step": "one (sequence, head) sample of the workload per step"},
-        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": os.cpu_count(),
+        "config": {"workload": w.name, "desc": w.note, **shape},
+        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": os.cpu_count(),
                          "kind": "oracle", "sample": sample},
-        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+        "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -470,7 +628,10 @@ def main():
         torch.cuda.set_device(local)
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     try:
-        run_ours(args, world, rank, local)
+        if args.workload in I.DECODE_WORKLOADS:
+            run_decode(args, world, rank, local)
+        else:
+            run_ours(args, world, rank, local)
     finally:
         if world > 1:
             import torch.distributed as dist

@@ -211,6 +211,80 @@ fa_status fa_bwd_stage(int stage, const void* q, const void* k, const void* v, c
                   workspace, workspace_bytes, stream);
 }
 
+// Decode: sizes valid and supported?  Fills the derived sizes.
+static fa_status decode_sizes(int B, int Hq, int Hkv, int S_max, int q_len, int d, int* R,
+                              int* chunk, int* nsplit) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || S_max < 0 || q_len <= 0 || d <= 0) return FA_ERR_SHAPE;
+  if (Hq % Hkv != 0) return FA_ERR_SHAPE;
+  if (B > 0 && q_len > S_max) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long rows = (long long)(Hq / Hkv) * q_len;
+  if (rows > fa::kDecodeMaxRows) return FA_ERR_UNSUPPORTED;
+  if ((long long)B * S_max >= (1ll << 31) || (long long)B * q_len * Hq >= (1ll << 31))
+    return FA_ERR_UNSUPPORTED;
+  *R = (int)rows;
+  *chunk = fa::decode_chunk(B, Hkv, S_max);
+  *nsplit = S_max > 0 ? (S_max + *chunk - 1) / *chunk : 0;
+  return FA_OK;
+}
+
+size_t fa_decode_workspace_size(int B, int Hq, int Hkv, int S_max, int q_len, int d) {
+  int R = 0, chunk = 0, nsplit = 0;
+  if (decode_sizes(B, Hq, Hkv, S_max, q_len, d, &R, &chunk, &nsplit) != FA_OK) return 0;
+  const size_t units = (size_t)B * Hkv * nsplit;
+  return round256(units * R * d * sizeof(float)) + round256(units * R * 2 * sizeof(float));
+}
+
+fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* cache_seqlens, void* o, float* lse, int B, int Hq, int Hkv,
+                    int S_max, int q_len, int d, float scale, int window,
+                    const float* alibi_slopes, fa_dtype o_dtype, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  int R = 0, chunk = 0, nsplit = 0;
+  fa_status st = decode_sizes(B, Hq, Hkv, S_max, q_len, d, &R, &chunk, &nsplit);
+  if (st != FA_OK) return st;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_UNSUPPORTED;
+  if (o_dtype != FA_FP32 && o_dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+  if (!q || !k_cache || !v_cache || !o || !lse) return FA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o))
+    return FA_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_ALIGN;
+  if (B == 0) return FA_OK;
+  const size_t need = fa_decode_workspace_size(B, Hq, Hkv, S_max, q_len, d);
+  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_ALIGN;
+  fa::DecodeParams p = {};
+  p.q = q;
+  p.k = k_cache;
+  p.v = v_cache;
+  p.o = o;
+  p.lse = lse;
+  p.seqlens = cache_seqlens;
+  p.alibi = alibi_slopes;
+  const size_t units = (size_t)B * Hkv * nsplit;
+  p.part_o = static_cast<float*>(workspace);
+  p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                       round256(units * R * d * sizeof(float)));
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.S_max = S_max;
+  p.q_len = q_len;
+  p.d = d;
+  p.group = Hq / Hkv;
+  p.R = R;
+  p.chunk = chunk;
+  p.nsplit = nsplit;
+  p.window = band_width(window, S_max);
+  p.o_f32 = o_dtype == FA_FP32;
+  p.scale = scale;
+  p.scale_log2 = scale * fa::kLog2e;
+  p.status = status_ptr();
+  if (!p.status) return FA_ERR_CUDA;
+  const int e = fa::launch_decode_bf16(p, stream);
+  return e == 0 ? FA_OK : FA_ERR_CUDA;
+}
+
 fa_status fa_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {
   if (limit_ns == 0 || limit_ns > 10000000000ull) return FA_ERR_UNSUPPORTED;
   unsigned int* status = status_ptr();

@@ -46,11 +46,52 @@ struct AttnParams {
   float scale_log2;            // scale * log2(e)
 };
 
+// Decode over a KV cache: the q_len newest tokens of each sequence attend to
+// its cache of cache_seqlens[b] tokens.  The keys of one (sequence, kv head)
+// are cut into chunks of `chunk`; one block computes the partial (m, l, O) of
+// one chunk for the R = group * q_len query rows of that kv head, and a
+// combine kernel merges the chunks.
+struct DecodeParams {
+  const void* q;               // bf16 [B * q_len, Hq, d]
+  const void* k;               // bf16 [B, S_max, Hkv, d]
+  const void* v;               // bf16 [B, S_max, Hkv, d]
+  void* o;                     // [B * q_len, Hq, d], fp32 or bf16
+  float* lse;                  // [Hq, B * q_len]
+  const int32_t* seqlens;      // [B] or nullptr (every cache holds S_max tokens)
+  const float* alibi;          // [Hq] or nullptr
+  float* part_o;               // [B, Hkv, nsplit, R, d] fp32: unnormalised partial O
+  float* part_ml;              // [B, Hkv, nsplit, R, 2] fp32: partial max (log2 units), sum
+  unsigned int* status;
+  int B, Hq, Hkv, S_max, q_len, d, group, R;
+  int chunk, nsplit;
+  int window;                  // kNoWindow when unbanded
+  int o_f32;
+  float scale, scale_log2;
+};
+
+// GB300 has 152 SMs; decode chunks are sized so that a batch of full caches
+// gives at least this many (sequence, kv head, chunk) blocks.
+constexpr int kDecodeUnitsTarget = 8 * 152;
+constexpr int kDecodeMaxRows = 16;
+
+// Keys per decode block: the largest of 64, 128, ..., 4096 that still leaves
+// kDecodeUnitsTarget blocks for B caches of S_max tokens.
+inline int decode_chunk(int B, int Hkv, int S_max) {
+  int c = 64;
+  while (c < 4096) {
+    const long long n = (long long)B * Hkv * ((S_max + 2 * c - 1) / (2 * c));
+    if (n < kDecodeUnitsTarget) break;
+    c *= 2;
+  }
+  return c;
+}
+
 // Launchers (each returns a cudaError_t value as int).
 int launch_fwd_fp32(const AttnParams& p, void* stream);
 int launch_fwd_bf16(const AttnParams& p, void* stream);
 int launch_bwd_bf16(const AttnParams& p, void* stream, int stage);   // stage < 0: all
 int launch_bwd_dq_bf16(const AttnParams& p, void* stream);            // deterministic dQ
+int launch_decode_bf16(const DecodeParams& p, void* stream);          // split + combine
 int launch_selftest_wait(unsigned int* status, unsigned long long limit_ns, void* stream);
 
 #ifdef __CUDACC__

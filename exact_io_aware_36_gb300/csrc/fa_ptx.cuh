@@ -169,6 +169,27 @@ __device__ __forceinline__ bool wait_warp_drain(uint64_t* bar, uint32_t parity) 
   }
 }
 
+// ---------------------------------------------------------- named barriers
+
+// Barrier `id` over the first `nthreads` threads (a multiple of 32) that
+// reach it; all of them must.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+
+// Barrier as above that also returns, to every participant, whether `pred`
+// held in any of them (barrier with OR reduction).
+__device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r) : "r"((uint32_t)pred), "r"(id), "r"(nthreads) : "memory");
+  return r != 0;
+}
+
 // ------------------------------------------------------------------ fences
 
 __device__ __forceinline__ void fence_proxy_async_smem() {

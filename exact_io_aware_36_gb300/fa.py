@@ -25,7 +25,8 @@ STATUS = {
     5: "FA_ERR_WORKSPACE", 6: "FA_ERR_CUDA", 7: "FA_ERR_DEVICE_TIMEOUT", 8: "FA_ERR_CU_SEQLENS",
 }
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_stage", "fa_bwd_workspace_size", "fa_check_device_error",
-           "fa_status_string", "fa_version", "fa_bwd_static_scratch", "fa_selftest_wait_timeout")
+           "fa_status_string", "fa_version", "fa_bwd_static_scratch", "fa_selftest_wait_timeout",
+           "fa_decode", "fa_decode_workspace_size")
 FA_BWD_PREPROCESS, FA_BWD_DKDV, FA_BWD_DQ_CONVERT = 0, 1, 2
 
 
@@ -63,6 +64,10 @@ def load(path: Optional[str] = None):
     lib.fa_bwd_stage.restype = i
     lib.fa_bwd_workspace_size.argtypes = [i, i, i, i, ll]
     lib.fa_bwd_workspace_size.restype = sz
+    lib.fa_decode_workspace_size.argtypes = [i, i, i, i, i, i]
+    lib.fa_decode_workspace_size.restype = sz
+    lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, i, vp, sz, vp]
+    lib.fa_decode.restype = i
     lib.fa_check_device_error.argtypes = [vp]
     lib.fa_check_device_error.restype = i
     lib.fa_status_string.argtypes = [i]
@@ -115,6 +120,17 @@ def fa_bwd_static_scratch(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, sca
         fn.restype = ctypes.c_int
     return fn(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, int(causal), int(window),
               cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype, int(deterministic), stream)
+
+
+def fa_decode_workspace_size(B, Hq, Hkv, S_max, q_len, d) -> int:
+    return load().fa_decode_workspace_size(B, Hq, Hkv, S_max, q_len, d)
+
+
+def fa_decode(q, k_cache, v_cache, cache_seqlens, o, lse, B, Hq, Hkv, S_max, q_len, d, scale,
+              window, alibi_slopes, o_dtype, workspace, workspace_bytes, stream) -> int:
+    return load().fa_decode(q, k_cache, v_cache, cache_seqlens, o, lse, B, Hq, Hkv, S_max, q_len,
+                            d, scale, int(window), alibi_slopes, o_dtype, workspace,
+                            workspace_bytes, stream)
 
 
 def fa_bwd_workspace_size(B, Hq, N, d, total_tokens) -> int:
@@ -237,3 +253,36 @@ def attention_backward(q, k, v, o, dO, lse, *, causal: bool, scale: Optional[flo
     if check:
         _check(fa_check_device_error(_stream(stream)), "fa_bwd (device)")
     return dq, dk, dv
+
+
+def attention_decode(q, k_cache, v_cache, *, cache_seqlens=None, q_len: int = 1,
+                     scale: Optional[float] = None, alibi_slopes=None,
+                     window: Optional[int] = None, out=None, lse=None, out_dtype=None,
+                     workspace=None, stream=None, check: bool = False):
+    """O, LSE of the q_len newest tokens of each sequence through ``fa_decode``.
+
+    q: bf16 [B * q_len, Hq, d]; k_cache, v_cache: bf16 [B, S_max, Hkv, d];
+    cache_seqlens: int32 [B] on the GPU (None: every cache holds S_max).
+    Returns (o [B * q_len, Hq, d] of ``out_dtype`` (default fp32), lse
+    float32 [Hq, B * q_len]).
+    """
+    import torch
+    B, S_max, Hkv, d = k_cache.shape
+    Hq = q.shape[1]
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype or torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((Hq, q.shape[0]), dtype=torch.float32, device=q.device)
+    need = fa_decode_workspace_size(B, Hq, Hkv, S_max, q_len, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = fa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_seqlens), _ptr(out), _ptr(lse),
+                   B, Hq, Hkv, S_max, q_len, d, float(scale), -1 if window is None else window,
+                   _ptr(alibi_slopes), _dtype_code(out.dtype), _ptr(workspace), workspace.numel(),
+                   _stream(stream))
+    _check(st, "fa_decode")
+    if check:
+        _check(fa_check_device_error(_stream(stream)), "fa_decode (device)")
+    return out, lse

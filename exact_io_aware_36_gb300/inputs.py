@@ -36,7 +36,8 @@ import numpy as np
 __all__ = [
     "Workload", "WORKLOADS", "EXTRA_WORKLOADS", "workload", "make_inputs", "small_case",
     "bf16_round", "bf16_bits", "bf16_from_bits", "alibi_slopes",
-    "attended_pairs",
+    "attended_pairs", "DecodeWorkload", "DECODE_WORKLOADS", "DecodeInputs",
+    "make_decode_inputs", "decode_bytes",
 ]
 
 
@@ -235,3 +236,97 @@ def make_inputs(w: Workload, seed: int = 0, with_do: Optional[bool] = None) -> I
 def with_seqlens(w: Workload, seqlens) -> Workload:
     return replace(w, seqlens=tuple(int(x) for x in seqlens), B=len(seqlens),
                    N=int(max(seqlens)), seqlen_range=None)
+
+
+# --------------------------------------------------------------------------
+# Decode over a KV cache: the q_len newest tokens of B sequences against
+# their caches [B, S_max, Hkv, d] of cache_seqlens[b] tokens.
+# --------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """One synthetic decode step.  Cache lengths are drawn uniformly from
+    ``len_range`` (closed), or given as ``lens``; ``S_max`` is the cache
+    capacity per sequence."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    S_max: int
+    d: int
+    q_len: int = 1
+    len_range: Optional[tuple] = None
+    lens: Optional[tuple] = None
+    alibi: bool = False
+    window: Optional[int] = None
+    note: str = ""
+
+    @property
+    def scale(self) -> float:
+        return float(1.0 / np.sqrt(self.d))
+
+    @property
+    def window_arg(self) -> int:
+        return -1 if self.window is None else int(self.window)
+
+
+DECODE_WORKLOADS = {
+    "decode_gqa": DecodeWorkload(
+        "decode_gqa", B=16, Hq=32, Hkv=8, S_max=32768, d=128, q_len=1, len_range=(1024, 32768),
+        note="decode step: 16 sequences, caches U[1024, 32768] tokens, GQA 32/8, d=128, bf16"),
+}
+
+
+@dataclass
+class DecodeInputs:
+    workload: DecodeWorkload
+    seed: int
+    seqlens: np.ndarray             # int32 [B]
+    q: np.ndarray                   # float32 [B * q_len, Hq, d], bf16-exact
+    q_bits: np.ndarray              # uint16, same shape
+    k_bits: np.ndarray              # uint16 [B, S_max, Hkv, d]
+    v_bits: np.ndarray
+    alibi_slopes: Optional[np.ndarray]
+    scale: float
+
+    def cache(self, name: str, seqs=None) -> np.ndarray:
+        """float32 copy of the k or v cache (bf16-exact), of the sequences
+        ``seqs`` (all when None)."""
+        bits = self.k_bits if name == "k" else self.v_bits
+        return bf16_from_bits(bits if seqs is None else bits[list(seqs)])
+
+
+def make_decode_inputs(w: DecodeWorkload, seed: int = 0) -> DecodeInputs:
+    """Draw a decode step: lengths first (when drawn), then q, then the k and v
+    caches one sequence at a time, all ``standard_normal(float32)`` rounded to
+    bf16.  Cache slots at or past a sequence's length hold drawn values that
+    attention never reads."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    if w.lens is not None:
+        lens = np.asarray(w.lens, dtype=np.int64)
+    elif w.len_range is not None:
+        lo, hi = w.len_range
+        lens = rng.integers(lo, hi + 1, size=w.B).astype(np.int64)
+    else:
+        lens = np.full(w.B, w.S_max, dtype=np.int64)
+    q = rng.standard_normal(size=(w.B * w.q_len, w.Hq, w.d), dtype=np.float32)
+    q_bits = bf16_bits(q)
+    q = bf16_from_bits(q_bits)
+    caches = []
+    for _ in ("k", "v"):
+        bits = np.empty((w.B, w.S_max, w.Hkv, w.d), dtype=np.uint16)
+        for b in range(w.B):
+            bits[b] = bf16_bits(rng.standard_normal(size=(w.S_max, w.Hkv, w.d), dtype=np.float32))
+        caches.append(bits)
+    slopes = alibi_slopes(w.Hq) if w.alibi else None
+    return DecodeInputs(w, seed, lens.astype(np.int32), q, q_bits, caches[0], caches[1], slopes,
+                        w.scale)
+
+
+def decode_bytes(w: DecodeWorkload, seqlens) -> int:
+    """HBM bytes one decode step must move: every cached key and value read
+    once (bf16), q read (bf16), O written (fp32) and LSE written."""
+    L = np.asarray(seqlens, dtype=np.int64)
+    kv = int(L.sum()) * w.Hkv * w.d * 2 * 2
+    rows = w.B * w.q_len * w.Hq
+    return kv + rows * w.d * 2 + rows * w.d * 4 + rows * 4

@@ -202,6 +202,41 @@ fa_status fa_bwd_static_scratch(const void* q, const void* k, const void* v, con
                                 int deterministic, void* stream);
 
 /*
+ * Decode over a KV cache: the q_len newest tokens of each sequence attend to
+ * that sequence's cached keys and values ("FlashAttention: Faster Attention
+ * Without Dropping a Single Interaction", Long context and inference: a tiny
+ * query scanning a growing cache).  Sequence b holds L_b = cache_seqlens[b]
+ * tokens, the q_len new ones included; query row i of b is the token at
+ * position L_b - q_len + i and sees keys j <= L_b - q_len + i (causal), with
+ * the ALiBi bias and sliding window of fa_fwd.  The result equals the last
+ * q_len rows of fa_fwd's causal attention over the whole sequence.  The keys
+ * are split into chunks processed in parallel and merged with the pages'
+ * (m, l, O) merge rule (Key design 2), so this call launches two kernels.
+ *   q             bf16 [B * q_len, Hq, d]: rows b*q_len .. b*q_len+q_len-1
+ *                 are sequence b's new tokens
+ *   k_cache,
+ *   v_cache       bf16 [B, S_max, Hkv, d]; slots at or past L_b are not read
+ *   cache_seqlens device int32 [B] with q_len <= L_b <= S_max, or NULL (every
+ *                 cache holds S_max tokens); a value out of range is reported
+ *                 on the device as FA_ERR_CU_SEQLENS
+ *   o             [B * q_len, Hq, d], o_dtype FA_FP32 or FA_BF16
+ *   lse           float32 [Hq, B * q_len] (natural log)
+ *   d             64 or 128; (Hq / Hkv) * q_len <= 16, else FA_ERR_UNSUPPORTED
+ *   window        as fa_fwd (< 0: none)
+ *   workspace     device, >= fa_decode_workspace_size bytes, 256-byte
+ *                 aligned; holds the per-chunk partial states
+ * All pointers are device pointers owned by the caller; bf16 tensors and o
+ * 16-byte aligned.  Errors as fa_fwd.
+ */
+size_t fa_decode_workspace_size(int B, int Hq, int Hkv, int S_max, int q_len, int d);
+
+fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* cache_seqlens, void* o, float* lse, int B, int Hq, int Hkv,
+                    int S_max, int q_len, int d, float scale, int window,
+                    const float* alibi_slopes, fa_dtype o_dtype, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status
  * word.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT, FA_ERR_CU_SEQLENS, or
  * FA_ERR_CUDA if the synchronisation itself failed.

@@ -91,3 +91,27 @@ def backward(x: I.Inputs, guard=True, check=True, out_dtype=None, deterministic=
         for b, _ in bufs:
             assert_guards(b)
     return as_f64(o), as_f64(lse), as_f64(dq), as_f64(dk), as_f64(dv)
+
+
+def bits_to_dev(bits: np.ndarray):
+    t = torch()
+    return t.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(t.bfloat16).cuda()
+
+
+def decode(x: I.DecodeInputs, guard=True, check=True, out_dtype=None, with_seqlens=True):
+    """Run fa_decode on inputs `x`; returns (O, LSE) as float64 numpy arrays.
+    O is stored as fp32 unless `out_dtype` says otherwise."""
+    t = torch()
+    w = x.workload
+    q, kc, vc = bits_to_dev(x.q_bits), bits_to_dev(x.k_bits), bits_to_dev(x.v_bits)
+    cs = t.from_numpy(x.seqlens.astype(np.int32)).cuda() if with_seqlens else None
+    slopes = t.from_numpy(x.alibi_slopes).cuda() if x.alibi_slopes is not None else None
+    obuf, o = guarded_empty(q.shape, out_dtype or t.float32)
+    lbuf, lse = guarded_empty((w.Hq, q.shape[0]), t.float32)
+    fa.attention_decode(q, kc, vc, cache_seqlens=cs, q_len=w.q_len, scale=x.scale,
+                        alibi_slopes=slopes, window=w.window, out=o, lse=lse, check=check)
+    t.cuda.synchronize()
+    if guard:
+        assert_guards(obuf)
+        assert_guards(lbuf)
+    return as_f64(o), as_f64(lse)

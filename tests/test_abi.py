@@ -113,3 +113,36 @@ def test_workspace_size(lib):
     assert n == r(Hq * T * 4) + r(Hq * T * d * 4)
     assert fa.fa_bwd_workspace_size(2, Hq, 4096, d, T) == n   # packed: T given
     assert fa.fa_bwd_workspace_size(-1, Hq, T, d, 0) == 0
+
+
+def dec(**kw):
+    a = dict(q=A, k=A, v=A, cs=None, o=A, lse=A, B=2, Hq=8, Hkv=2, S=4096, ql=1, d=128,
+             scale=0.088, window=-1, alibi=None, odt=fa.FA_FP32, ws=A, wsb=1 << 40, stream=None)
+    a.update(kw)
+    return fa.fa_decode(a["q"], a["k"], a["v"], a["cs"], a["o"], a["lse"], a["B"], a["Hq"],
+                        a["Hkv"], a["S"], a["ql"], a["d"], a["scale"], a["window"], a["alibi"],
+                        a["odt"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(k=None), 1), (dict(lse=None), 1),
+    (dict(Hq=6, Hkv=4), 2), (dict(B=-1), 2), (dict(ql=0), 2), (dict(S=-1), 2),
+    (dict(ql=5000), 2),                          # more new tokens than the cache holds
+    (dict(d=96), 3), (dict(Hq=32, Hkv=1), 3),    # 32 rows per kv head > 16
+    (dict(Hq=8, Hkv=2, ql=5), 3), (dict(scale=0.0), 3), (dict(odt=4), 3),
+    (dict(q=A + 8), 4), (dict(o=A + 4), 4), (dict(ws=A + 16), 4),
+    (dict(ws=None), 5), (dict(wsb=1000), 5),
+    (dict(B=0), 0),
+])
+def test_decode_rejects_before_launch(lib, kw, code):
+    assert dec(**kw) == code
+
+
+def test_decode_workspace_size(lib):
+    from exact_io_aware_36_gb300 import inputs as I  # noqa: F401  (import check only)
+    n = fa.fa_decode_workspace_size(16, 32, 8, 32768, 1, 128)
+    # 16 x 8 (sequence, kv head) pairs, chunks of 2048 keys -> 16 chunks; R = 4 rows
+    units = 16 * 8 * 16
+    assert n == units * 4 * 128 * 4 + ((units * 4 * 2 * 4 + 255) // 256) * 256
+    assert fa.fa_decode_workspace_size(1, 3, 2, 64, 1, 64) == 0      # Hq % Hkv != 0
+    assert fa.fa_decode_workspace_size(1, 32, 1, 64, 1, 64) == 0     # 32 rows
