@@ -58,6 +58,8 @@ def parse():
                     sorted(I.DECODE_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time the FP8 forward (quantize + e4m3 attention) on the workload")
     ap.add_argument("--deterministic", action="store_true",
                     help="time the deterministic backward (dQ by its own kernel, no atomics)")
     return ap.parse_args()
@@ -340,6 +342,114 @@ def run_decode(args, world, rank, local):
         "clocks": clocks,
         "e2e": e2e,
         "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------- fp8
+
+FP8_METRIC = "FP8 (e4m3) attention forward TFLOP/s on 1 GB300 (quantize + attention)"
+FP8_OVER_BF16 = 2.0        # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
+
+
+def run_fp8(args, world, rank, local):
+    """One step = fa_fp8_quantize (incoherent transform, per-block e4m3 codes)
+    then fa_fwd_fp8 over the workload; FLOPs are the forward's 4 d per pair."""
+    import torch
+    from exact_io_aware_36_gb300 import fa
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = I.workload(args.workload)
+    x = I.make_inputs(w, seed=0, with_do=False)
+    fl = flops_per_step(w, x.seqlens)["fwd"]
+    T = x.T
+
+    def todev(name):
+        return torch.from_numpy(x.bits[name].view("int16")).view(torch.bfloat16).to(dev)
+
+    q, k, v = todev("q"), todev("k"), todev("v")
+    signs = torch.from_numpy(I.hadamard_signs(w.d, seed=0)).to(dev)
+    cu = torch.from_numpy(x.cu_seqlens).to(dev) if w.varlen else None
+    slopes = torch.from_numpy(x.alibi_slopes).to(dev) if w.alibi else None
+    o = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    lse = torch.empty((w.Hq, T), dtype=torch.float32, device=dev)
+    st, lay = fa.fa_fp8_layout_get(w.B, w.Hq, w.Hkv, w.N, w.d, T if w.varlen else 0)
+    if st:
+        raise fa.FAError(st, "fa_fp8_layout_get")
+    buf = torch.empty(lay.total, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    P = lambda t: None if t is None else t.data_ptr()
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        r = fa.fa_fp8_quantize(P(q), P(k), P(v), P(signs), w.B, w.Hq, w.Hkv, w.N, w.d, P(cu), T,
+                               P(buf), lay.total, sp)
+        if r:
+            raise fa.FAError(r, "fa_fp8_quantize")
+        if evs is not None:
+            evs[1].record(stream)
+        r = fa.fa_fwd_fp8(P(buf), lay.total, P(o), P(lse), w.B, w.Hq, w.Hkv, w.N, w.d,
+                          float(x.scale), int(w.causal), w.window_arg, P(cu), T, P(slopes),
+                          fa.FA_FP32, sp)
+        if r:
+            raise fa.FAError(r, "fa_fwd_fp8")
+        if evs is not None:
+            evs[2].record(stream)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.fa_check_device_error(sp):
+        raise fa.FAError(7, "warm-up")
+    evsets = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(smi_index(local))
+    sampler.start()
+    time.sleep(0.1)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        step(evsets[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    st = fa.fa_check_device_error(sp)
+    if st:
+        raise fa.FAError(st, "timed region")
+    ms_step = max_over_ranks(start.elapsed_time(end), world, dev) / args.steps
+    value = job_throughput(fl, ms_step, world)
+    q_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evsets)
+    a_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evsets)
+    bf16_peak, _, src = load_peaks()
+    peak = bf16_peak * FP8_OVER_BF16
+    ach = fl / (a_ms * 1e-3) / 1e12
+    line = {
+        "metric": FP8_METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic (seeded PCG64, seed 0; no dataset)",
+        "config": {"workload": w.name, "desc": w.note, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "N": w.N, "d": w.d, "causal": w.causal, "window": w.window, "alibi": w.alibi,
+                   "varlen": w.varlen, "o_dtype": "fp32", "flops_per_step": fl,
+                   "attention_only_tflops": round(ach, 1), "l2": l2_note(w, T),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "per_kernel": {"fp8_quantize": {"ms": round(q_ms, 4), "share": round(q_ms / (q_ms + a_ms), 4)},
+                       "fwd_fp8": {"ms": round(a_ms, 4), "tflops": round(ach, 1),
+                                   "share": round(a_ms / (q_ms + a_ms), 4)}},
+        "roofline": {"kernel": "fwd_fp8", "bound": "tensor", "achieved": round(ach, 1),
+                     "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+                     "peak_source": f"{src} bf16 burst x {FP8_OVER_BF16:g} (nominal e4m3 / bf16 ratio)",
+                     "traffic": ncu_traffic(w.name + " fp8", "fwd_fp8")},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks, "e2e": None, "cpu_baseline": None,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -630,6 +740,8 @@ def main():
     try:
         if args.workload in I.DECODE_WORKLOADS:
             run_decode(args, world, rank, local)
+        elif args.fp8:
+            run_fp8(args, world, rank, local)
         else:
             run_ours(args, world, rank, local)
     finally:

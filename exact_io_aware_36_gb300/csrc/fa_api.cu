@@ -285,6 +285,114 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache,
   return e == 0 ? FA_OK : FA_ERR_CUDA;
 }
 
+fa_status fa_fp8_layout_get(int B, int Hq, int Hkv, int N, int d, long long total_tokens,
+                            fa_fp8_layout* out) {
+  if (!out) return FA_ERR_NULL;
+  if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || total_tokens < 0) return FA_ERR_SHAPE;
+  if (Hq % Hkv != 0) return FA_ERR_SHAPE;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  const long long T = total_tokens > 0 ? total_tokens : (long long)B * N;
+  const long long nblk = ((long long)N + 127) / 128;
+  const long long vt = (long long)B * nblk * 128;      // keys per transposed V row
+  // token and key coordinates are 32-bit in the TMA descriptors
+  if (T >= (1ll << 31) || vt >= (1ll << 31) || (long long)N >= (1ll << 30)) return FA_ERR_UNSUPPORTED;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = round256(off + bytes);
+    return at;
+  };
+  out->q8 = take((size_t)T * Hq * 128);
+  out->k8 = take((size_t)T * Hkv * 128);
+  out->v8t = take((size_t)Hkv * 128 * vt);
+  out->q_scale = take(sizeof(float) * Hq * B * nblk);
+  out->k_scale = take(sizeof(float) * Hkv * B * nblk);
+  out->v_scale = take(sizeof(float) * Hkv * B * nblk);
+  out->v_scale_max = take(sizeof(float) * Hkv);
+  out->total = off;
+  out->nblk = (int)nblk;
+  return FA_OK;
+}
+
+fa_status fa_fp8_quantize(const void* q, const void* k, const void* v, const float* signs,
+                          int B, int Hq, int Hkv, int N, int d, const int32_t* cu_seqlens,
+                          long long total_tokens, void* fp8_buf, size_t fp8_bytes, void* stream) {
+  long long T = 0;
+  fa_status st = check_sizes(B, Hq, Hkv, N, d, 1.0f, cu_seqlens, total_tokens, FA_BF16, false, &T);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !signs) return FA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return FA_ERR_ALIGN;
+  if (T == 0 || B == 0 || N == 0) return FA_OK;
+  fa_fp8_layout lay;
+  st = fa_fp8_layout_get(B, Hq, Hkv, N, d, cu_seqlens ? T : 0, &lay);
+  if (st != FA_OK) return st;
+  if (!fp8_buf || fp8_bytes < lay.total) return FA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(fp8_buf) & 255u) != 0) return FA_ERR_ALIGN;
+  char* base = static_cast<char*>(fp8_buf);
+  fa::QuantParams p = {};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.signs = signs;
+  p.cu_seqlens = cu_seqlens;
+  p.q8 = reinterpret_cast<uint8_t*>(base + lay.q8);
+  p.k8 = reinterpret_cast<uint8_t*>(base + lay.k8);
+  p.v8t = reinterpret_cast<uint8_t*>(base + lay.v8t);
+  p.q_scale = reinterpret_cast<float*>(base + lay.q_scale);
+  p.k_scale = reinterpret_cast<float*>(base + lay.k_scale);
+  p.v_scale = reinterpret_cast<float*>(base + lay.v_scale);
+  p.v_smax = reinterpret_cast<float*>(base + lay.v_scale_max);
+  p.T = T;
+  p.vt_stride = (long long)B * lay.nblk * 128;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.nblk = lay.nblk;
+  p.status = status_ptr();
+  if (!p.status) return FA_ERR_CUDA;
+  return fa::launch_fp8_quantize(p, stream) == 0 ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_fwd_fp8(const void* fp8_buf, size_t fp8_bytes, void* o, float* lse, int B, int Hq,
+                     int Hkv, int N, int d, float scale, int causal, int window,
+                     const int32_t* cu_seqlens, long long total_tokens,
+                     const float* alibi_slopes, fa_dtype o_dtype, void* stream) {
+  long long T = 0;
+  fa_status st = check_sizes(B, Hq, Hkv, N, d, scale, cu_seqlens, total_tokens, FA_BF16, false, &T);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (window >= 0 && !causal) return FA_ERR_UNSUPPORTED;
+  if (o_dtype != FA_FP32 && o_dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+  if (!fp8_buf || !o || !lse) return FA_ERR_NULL;
+  if (!aligned16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(fp8_buf) & 255u) != 0) return FA_ERR_ALIGN;
+  if (T == 0 || B == 0 || N == 0) return FA_OK;
+  fa_fp8_layout lay;
+  st = fa_fp8_layout_get(B, Hq, Hkv, N, d, cu_seqlens ? T : 0, &lay);
+  if (st != FA_OK) return st;
+  if (fp8_bytes < lay.total) return FA_ERR_WORKSPACE;
+  const char* base = static_cast<const char*>(fp8_buf);
+  fa::AttnParams p = base_params(B, Hq, Hkv, N, d, scale, causal, window, cu_seqlens, T,
+                                 alibi_slopes);
+  p.q = base + lay.q8;
+  p.k = base + lay.k8;
+  p.v = base + lay.v8t;
+  p.q_scale = reinterpret_cast<const float*>(base + lay.q_scale);
+  p.k_scale = reinterpret_cast<const float*>(base + lay.k_scale);
+  p.v_scale = reinterpret_cast<const float*>(base + lay.v_scale);
+  p.v_smax = reinterpret_cast<const float*>(base + lay.v_scale_max);
+  p.nblk = lay.nblk;
+  p.vt_stride = (long long)B * lay.nblk * 128;
+  p.o = o;
+  p.lse = lse;
+  p.o_f32 = o_dtype == FA_FP32;
+  p.status = status_ptr();
+  if (!p.status) return FA_ERR_CUDA;
+  return fa::launch_fwd_fp8(p, stream) == 0 ? FA_OK : FA_ERR_CUDA;
+}
+
 fa_status fa_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {
   if (limit_ns == 0 || limit_ns > 10000000000ull) return FA_ERR_UNSUPPORTED;
   unsigned int* status = status_ptr();

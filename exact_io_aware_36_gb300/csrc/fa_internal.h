@@ -44,6 +44,33 @@ struct AttnParams {
   int o_f32;                    // o stored as fp32 (else the input dtype)
   float scale;
   float scale_log2;            // scale * log2(e)
+  // FP8 forward: per-block scales ([H, B * nblk]) and the largest V scale
+  // of each kv head; q, k are the e4m3 codes, v the transposed V codes
+  const float* q_scale;
+  const float* k_scale;
+  const float* v_scale;
+  const float* v_smax;
+  int nblk;
+  long long vt_stride;         // bytes per row of the transposed V codes
+};
+
+// FP8 quantization (Q' = (Q D) H, K' = (K D) H, V; e4m3 per 128-row block).
+struct QuantParams {
+  const void* q;               // bf16 [T, Hq, 128]
+  const void* k;               // bf16 [T, Hkv, 128]
+  const void* v;               // bf16 [T, Hkv, 128]
+  const float* signs;          // [128], +-1
+  const int32_t* cu_seqlens;
+  unsigned int* status;
+  uint8_t* q8;
+  uint8_t* k8;
+  uint8_t* v8t;
+  float* q_scale;
+  float* k_scale;
+  float* v_scale;
+  float* v_smax;
+  long long T, vt_stride;
+  int B, Hq, Hkv, N, nblk;
 };
 
 // Decode over a KV cache: the q_len newest tokens of each sequence attend to
@@ -92,6 +119,8 @@ int launch_fwd_bf16(const AttnParams& p, void* stream);
 int launch_bwd_bf16(const AttnParams& p, void* stream, int stage);   // stage < 0: all
 int launch_bwd_dq_bf16(const AttnParams& p, void* stream);            // deterministic dQ
 int launch_decode_bf16(const DecodeParams& p, void* stream);          // split + combine
+int launch_fp8_quantize(const QuantParams& p, void* stream);
+int launch_fwd_fp8(const AttnParams& p, void* stream);
 int launch_selftest_wait(unsigned int* status, unsigned long long limit_ns, void* stream);
 
 #ifdef __CUDACC__

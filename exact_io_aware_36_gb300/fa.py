@@ -26,7 +26,8 @@ STATUS = {
 }
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_stage", "fa_bwd_workspace_size", "fa_check_device_error",
            "fa_status_string", "fa_version", "fa_bwd_static_scratch", "fa_selftest_wait_timeout",
-           "fa_decode", "fa_decode_workspace_size")
+           "fa_decode", "fa_decode_workspace_size", "fa_fp8_layout_get", "fa_fp8_quantize",
+           "fa_fwd_fp8")
 FA_BWD_PREPROCESS, FA_BWD_DKDV, FA_BWD_DQ_CONVERT = 0, 1, 2
 
 
@@ -43,6 +44,14 @@ class FAError(RuntimeError):
 
 
 _lib = None
+
+
+class FP8Layout(ctypes.Structure):
+    """fa_fp8_layout: byte offsets of the FP8 codes and scales in one buffer."""
+    _fields_ = [("q8", ctypes.c_size_t), ("k8", ctypes.c_size_t), ("v8t", ctypes.c_size_t),
+                ("q_scale", ctypes.c_size_t), ("k_scale", ctypes.c_size_t),
+                ("v_scale", ctypes.c_size_t), ("v_scale_max", ctypes.c_size_t),
+                ("total", ctypes.c_size_t), ("nblk", ctypes.c_int)]
 
 
 def load(path: Optional[str] = None):
@@ -68,6 +77,12 @@ def load(path: Optional[str] = None):
     lib.fa_decode_workspace_size.restype = sz
     lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, i, vp, sz, vp]
     lib.fa_decode.restype = i
+    lib.fa_fp8_layout_get.argtypes = [i, i, i, i, i, ll, ctypes.POINTER(FP8Layout)]
+    lib.fa_fp8_layout_get.restype = i
+    lib.fa_fp8_quantize.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp, ll, vp, sz, vp]
+    lib.fa_fp8_quantize.restype = i
+    lib.fa_fwd_fp8.argtypes = [vp, sz, vp, vp, i, i, i, i, i, f, i, i, vp, ll, vp, i, vp]
+    lib.fa_fwd_fp8.restype = i
     lib.fa_check_device_error.argtypes = [vp]
     lib.fa_check_device_error.restype = i
     lib.fa_status_string.argtypes = [i]
@@ -131,6 +146,25 @@ def fa_decode(q, k_cache, v_cache, cache_seqlens, o, lse, B, Hq, Hkv, S_max, q_l
     return load().fa_decode(q, k_cache, v_cache, cache_seqlens, o, lse, B, Hq, Hkv, S_max, q_len,
                             d, scale, int(window), alibi_slopes, o_dtype, workspace,
                             workspace_bytes, stream)
+
+
+def fa_fp8_layout_get(B, Hq, Hkv, N, d, total_tokens):
+    """(status, FP8Layout)."""
+    lay = FP8Layout()
+    st = load().fa_fp8_layout_get(B, Hq, Hkv, N, d, total_tokens, ctypes.byref(lay))
+    return st, lay
+
+
+def fa_fp8_quantize(q, k, v, signs, B, Hq, Hkv, N, d, cu_seqlens, total_tokens, fp8_buf,
+                    fp8_bytes, stream) -> int:
+    return load().fa_fp8_quantize(q, k, v, signs, B, Hq, Hkv, N, d, cu_seqlens, total_tokens,
+                                  fp8_buf, fp8_bytes, stream)
+
+
+def fa_fwd_fp8(fp8_buf, fp8_bytes, o, lse, B, Hq, Hkv, N, d, scale, causal, window, cu_seqlens,
+               total_tokens, alibi_slopes, o_dtype, stream) -> int:
+    return load().fa_fwd_fp8(fp8_buf, fp8_bytes, o, lse, B, Hq, Hkv, N, d, scale, int(causal),
+                             int(window), cu_seqlens, total_tokens, alibi_slopes, o_dtype, stream)
 
 
 def fa_bwd_workspace_size(B, Hq, N, d, total_tokens) -> int:
@@ -286,3 +320,37 @@ def attention_decode(q, k_cache, v_cache, *, cache_seqlens=None, q_len: int = 1,
     if check:
         _check(fa_check_device_error(_stream(stream)), "fa_decode (device)")
     return out, lse
+
+
+def attention_forward_fp8(q, k, v, signs, *, causal: bool, scale: Optional[float] = None,
+                          cu_seqlens=None, max_seqlen: Optional[int] = None,
+                          batch: Optional[int] = None, alibi_slopes=None,
+                          window: Optional[int] = None, out=None, lse=None, out_dtype=None,
+                          fp8_buf=None, stream=None, check: bool = False):
+    """O, LSE through ``fa_fp8_quantize`` and ``fa_fwd_fp8`` (d = 128).
+
+    q: bf16 [T, Hq, 128], k/v: bf16 [T, Hkv, 128]; signs: float32 [128] of
+    +-1 on the GPU.  Returns (o, lse, fp8_buf, layout): the buffer holds the
+    codes and scales at the layout's offsets.
+    """
+    import torch
+    T, B, Hq, Hkv, N, d = _sizes(q, k, cu_seqlens, max_seqlen, batch)
+    if scale is None:
+        scale = d ** -0.5
+    st, lay = fa_fp8_layout_get(B, Hq, Hkv, N, d, T if cu_seqlens is not None else 0)
+    _check(st, "fa_fp8_layout_get")
+    if fp8_buf is None:
+        fp8_buf = torch.empty(max(lay.total, 1), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype or torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
+    sp = _stream(stream)
+    _check(fa_fp8_quantize(_ptr(q), _ptr(k), _ptr(v), _ptr(signs), B, Hq, Hkv, N, d,
+                           _ptr(cu_seqlens), T, _ptr(fp8_buf), fp8_buf.numel(), sp), "fa_fp8_quantize")
+    _check(fa_fwd_fp8(_ptr(fp8_buf), fp8_buf.numel(), _ptr(out), _ptr(lse), B, Hq, Hkv, N, d,
+                      float(scale), causal, -1 if window is None else window, _ptr(cu_seqlens), T,
+                      _ptr(alibi_slopes), _dtype_code(out.dtype), sp), "fa_fwd_fp8")
+    if check:
+        _check(fa_check_device_error(sp), "fa_fwd_fp8 (device)")
+    return out, lse, fp8_buf, lay

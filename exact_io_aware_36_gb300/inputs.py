@@ -37,7 +37,7 @@ __all__ = [
     "Workload", "WORKLOADS", "EXTRA_WORKLOADS", "workload", "make_inputs", "small_case",
     "bf16_round", "bf16_bits", "bf16_from_bits", "alibi_slopes",
     "attended_pairs", "DecodeWorkload", "DECODE_WORKLOADS", "DecodeInputs",
-    "make_decode_inputs", "decode_bytes",
+    "make_decode_inputs", "decode_bytes", "hadamard_signs",
 ]
 
 
@@ -330,3 +330,10 @@ def decode_bytes(w: DecodeWorkload, seqlens) -> int:
     kv = int(L.sum()) * w.Hkv * w.d * 2 * 2
     rows = w.B * w.q_len * w.Hq
     return kv + rows * w.d * 2 + rows * w.d * 4 + rows * 4
+
+
+def hadamard_signs(d: int, seed: int = 0) -> np.ndarray:
+    """The random diagonal of the FP8 path's transform: float32 [d] of +-1,
+    from its own PCG64(seed) generator (one uniform draw per entry)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return np.where(rng.random(d) < 0.5, -1.0, 1.0).astype(np.float32)

@@ -237,6 +237,56 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache,
                     size_t workspace_bytes, void* stream);
 
 /*
+ * FP8 forward ("FlashAttention: Faster Attention Without Dropping a Single
+ * Interaction", FA3: per-block quantization and the same random orthogonal
+ * Hadamard transform on Q and K, so that (QM)(KM)^T = QK^T before
+ * quantization; the result is not exact).  Two calls:
+ *   fa_fp8_quantize  Q' = (Q D) H and K' = (K D) H with D = diag(signs) and
+ *                    H the unnormalised d x d Sylvester Hadamard matrix (the
+ *                    butterfly in float32); then Q', K' and V are quantized
+ *                    to e4m3 per block of 128 rows of one head of one
+ *                    sequence, scale = amax / 448 (1 for an all-zero block),
+ *                    code = e4m3(x / scale), round to nearest even, saturated.
+ *   fa_fwd_fp8       attention from those codes: S = scale * s_q * s_k
+ *                    * (Q8 K8^T) / d, the online softmax of fa_fwd, P rounded
+ *                    to e4m3 for the P V product (tensor cores, kind f8f6f4,
+ *                    fp32 accumulation); o and lse as fa_fwd.
+ * Only d = 128.  The codes and scales live in one caller-owned device buffer
+ * laid out as below (byte offsets from its start, each 256-byte aligned);
+ * nblk = ceil(N / 128); block i of sequence b has index b * nblk + i.
+ */
+typedef struct {
+  size_t q8;           /* uint8 [T, Hq, 128]: codes of Q' */
+  size_t k8;           /* uint8 [T, Hkv, 128]: codes of K' */
+  size_t v8t;          /* uint8 [Hkv, 128, B * nblk * 128]: codes of V transposed; key r
+                          of block (b, i) at column (b * nblk + i) * 128 + r; padding 0 */
+  size_t q_scale;      /* float32 [Hq, B * nblk] (1 where a block is empty) */
+  size_t k_scale;      /* float32 [Hkv, B * nblk] */
+  size_t v_scale;      /* float32 [Hkv, B * nblk] */
+  size_t v_scale_max;  /* float32 [Hkv]: the largest v_scale of each kv head */
+  size_t total;        /* bytes of the whole buffer */
+  int nblk;
+} fa_fp8_layout;
+
+/* Fills *out for a problem (sizes as fa_fwd; d must be 128). */
+fa_status fa_fp8_layout_get(int B, int Hq, int Hkv, int N, int d, long long total_tokens,
+                            fa_fp8_layout* out);
+
+/* q, k, v: bf16 as fa_fwd; signs: device float32 [d], each +1 or -1 (the
+ * random diagonal D, drawn by the caller); fp8_buf: device, >= total bytes,
+ * 256-byte aligned.  Launches three kernels on `stream`. */
+fa_status fa_fp8_quantize(const void* q, const void* k, const void* v, const float* signs,
+                          int B, int Hq, int Hkv, int N, int d, const int32_t* cu_seqlens,
+                          long long total_tokens, void* fp8_buf, size_t fp8_bytes, void* stream);
+
+/* Attention from the buffer fa_fp8_quantize filled (same sizes, cu_seqlens
+ * and d); other arguments as fa_fwd. */
+fa_status fa_fwd_fp8(const void* fp8_buf, size_t fp8_bytes, void* o, float* lse, int B, int Hq,
+                     int Hkv, int N, int d, float scale, int causal, int window,
+                     const int32_t* cu_seqlens, long long total_tokens,
+                     const float* alibi_slopes, fa_dtype o_dtype, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status
  * word.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT, FA_ERR_CU_SEQLENS, or
  * FA_ERR_CUDA if the synchronisation itself failed.
