@@ -232,7 +232,7 @@ size_t fa_decode_workspace_size(int B, int Hq, int Hkv, int S_max, int q_len, in
   int R = 0, chunk = 0, nsplit = 0;
   if (decode_sizes(B, Hq, Hkv, S_max, q_len, d, &R, &chunk, &nsplit) != FA_OK) return 0;
   const size_t units = (size_t)B * Hkv * nsplit;
-  return round256(units * R * d * sizeof(float)) + round256(units * R * 2 * sizeof(float));
+  return round256(units * R * d * sizeof(float)) + round256(units * R * 3 * sizeof(float));
 }
 
 fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache,

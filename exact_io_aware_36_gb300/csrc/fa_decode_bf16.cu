@@ -119,12 +119,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   const int kmin = max(k0, pos0 - W);           // lowest key any row of the block sees
   const int R = p.R;
   float* po = p.part_o + (long long)blockIdx.x * R * D;
-  float* pml = p.part_ml + (long long)blockIdx.x * R * 2;
+  float* pml = p.part_ml + (long long)blockIdx.x * R * 3;
   if (kmin >= k1) {                             // chunk below every row's window: empty state
     for (int i = threadIdx.x; i < R * D; i += blockDim.x) po[i] = 0.f;
     if (threadIdx.x < R) {
-      pml[2 * threadIdx.x] = -INFINITY;
-      pml[2 * threadIdx.x + 1] = 0.f;
+      pml[3 * threadIdx.x] = -INFINITY;
+      pml[3 * threadIdx.x + 1] = 0.f;
+      pml[3 * threadIdx.x + 2] = 0.f;
     }
     return;
   }
@@ -356,11 +357,389 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     }
     po[r * D + c] = o;
     if (c == 0) {
-      pml[2 * r] = M;
-      pml[2 * r + 1] = l;
+      pml[3 * r] = M;
+      pml[3 * r + 1] = l;      // P in fp32: the product used exactly these weights
+      pml[3 * r + 2] = l;
     }
   }
 }
+
+// ---------------------------------------------------------------------------
+// d = 128: the two products on the tensor cores, in transposed form so that
+// the keys, not the few query rows, fill the 128-row M of tcgen05:
+//   S^T(j) = K_j Q^T    M 128 keys, N 16 (query rows, zero-padded), K d
+//   O^T   += V_j^T P^T   M 128 head dims, N 16, K 128 keys (A = V_j as an
+//                        MN-major operand, B = P from shared memory)
+// Block (192 threads): warp 5 TMA, warp 4 MMA (one lane), warps 0-3 the
+// softmax with one key of the tile per thread.  The reference max of every
+// row is raised speculatively: a tile whose scores stay within tau of it
+// (the common case) needs no max at all; otherwise the block takes the exact
+// tile max (one vote and one exchange) and rescales its O^T rows in TMEM
+// once the previous product is complete.  P goes to shared memory in bf16;
+// the block's partial state is (m, l, l~) with l the exact sum of P and l~ the
+// sum of the rounded P the product used.
+// TMEM: S^T buffers at columns 0 and 16, O^T at 32 (16 columns each).
+namespace tc {
+
+constexpr int kThreads = 192;
+constexpr int kMmaWarp = 4;
+constexpr int kLoadWarp = 5;
+constexpr int kStages = 3;
+constexpr int kN = 16;                              // query rows per block, padded
+constexpr float kTau = 8.0f;
+constexpr int BOX = 128 * 64 * 2;                   // 128 keys x 64 head dims
+constexpr int TILE = 2 * BOX;                       // 128 keys x 128 head dims
+constexpr int QBOX = kN * 128;                      // 16 rows x 64 head dims (bf16)
+constexpr int PBOX = kN * 128;                      // 16 rows x 64 keys (bf16)
+constexpr int K_OFF = 0;
+constexpr int V_OFF = K_OFF + kStages * TILE;
+constexpr int Q_OFF = V_OFF + kStages * TILE;       // 2 boxes
+constexpr int P_OFF = Q_OFF + 2 * QBOX;             // 2 buffers x 2 boxes
+constexpr int RED_OFF = P_OFF + 4 * PBOX;           // float [8][16]: per-warp row maxima / sums
+constexpr int ROW_OFF = RED_OFF + 8 * kN * 4;       // int pos[16], float slope2[16]
+constexpr int BAR_OFF = ROW_OFF + 2 * kN * 4;
+constexpr int SMEM_BYTES = BAR_OFF + 128 + 1024;
+constexpr uint32_t S_COL = 0, O_COL = 32;
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t s_full[2], p_full[2];
+  uint64_t pv_done[2];       // PV(j) completes pv_done[j & 1]: waited in order, no phase skipped
+  uint64_t o_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(Bars) <= 128, "barrier block");
+
+__global__ void __launch_bounds__(kThreads, 1)
+decode_split_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
+  constexpr int D = 128;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  Bars* bars = reinterpret_cast<Bars*>(smem + BAR_OFF);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const int s = (int)(blockIdx.x % (unsigned)p.nsplit);
+  const int bg = (int)(blockIdx.x / (unsigned)p.nsplit);
+  const int g = bg % p.Hkv;
+  const int b = bg / p.Hkv;
+  const int L = p.seqlens ? __ldg(p.seqlens + b) : p.S_max;
+  if (L < p.q_len || L > p.S_max) {
+    if (threadIdx.x == 0) record_status(p.status, FA_ERR_CU_SEQLENS);
+    return;
+  }
+  const int k0 = s * p.chunk;
+  if (k0 >= L) return;                          // past this cache's end: no partial
+  const int k1 = min(k0 + p.chunk, L);
+  const int W = p.window;
+  const int pos0 = L - p.q_len;
+  const int kmin = max(k0, pos0 - W);
+  const int R = p.R;
+  float* po = p.part_o + (long long)blockIdx.x * R * D;
+  float* pml = p.part_ml + (long long)blockIdx.x * R * 3;
+  if (kmin >= k1) {                             // chunk below every row's window: empty state
+    for (int i = threadIdx.x; i < R * D; i += blockDim.x) po[i] = 0.f;
+    if (threadIdx.x < R) {
+      pml[3 * threadIdx.x] = -INFINITY;
+      pml[3 * threadIdx.x + 1] = 0.f;
+      pml[3 * threadIdx.x + 2] = 0.f;
+    }
+    return;
+  }
+  const int n = (k1 - kmin + 127) / 128;
+
+  int* rpos = reinterpret_cast<int*>(smem + ROW_OFF);
+  float* rslope = reinterpret_cast<float*>(smem + ROW_OFF + kN * 4);
+  float* red = reinterpret_cast<float*>(smem + RED_OFF);
+  // Q rows R..15 are zero (the TMA box fills rows 0..R-1 only)
+  for (int i = threadIdx.x; i < 2 * QBOX / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(smem + Q_OFF)[i] = make_uint4(0, 0, 0, 0);
+  if (threadIdx.x < kN) {
+    const int r = threadIdx.x < R ? threadIdx.x : 0;
+    rpos[threadIdx.x] = pos0 + r / p.group;
+    rslope[threadIdx.x] = p.alibi ? __ldg(p.alibi + g * p.group + r % p.group) * kLog2e : 0.f;
+  }
+  fence_proxy_async_smem();
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&bars->kv_full[i], 1);
+      mbar_init(&bars->kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->p_full[i], 4);
+    }
+    mbar_init(&bars->pv_done[0], 1);
+    mbar_init(&bars->pv_done[1], 1);
+    mbar_init(&bars->o_done, 1);
+    bars->abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&bars->tmem_base, 64);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const WaitCtx wc{&bars->abort_flag, p.status};
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      // the block's R rows: q_len tokens x group heads, row r = qi * group + hg
+      mbar_arrive_expect_tx(&bars->q_full, 2 * R * 128);
+      for (int bx = 0; bx < 2; ++bx)
+        tma_load_3d(smem + Q_OFF + bx * QBOX, &tmQ, bx * 64, g * p.group, b * p.q_len, &bars->q_full);
+    }
+    __syncwarp();
+    int issued = 0;
+    for (int j = 0; j < n; ++j) {
+      const int st = j % kStages;
+      if (!wait_warp(&bars->kv_empty[st], ((j / kStages) & 1) ^ 1, wc)) break;
+      if (lane == 0) {
+        const int row = b * p.S_max + kmin + 128 * j;
+        mbar_arrive_expect_tx(&bars->kv_full[st], 2 * TILE);
+        for (int bx = 0; bx < 2; ++bx) {
+          tma_load_3d(smem + K_OFF + st * TILE + bx * BOX, &tmK, bx * 64, g, row, &bars->kv_full[st]);
+          tma_load_3d(smem + V_OFF + st * TILE + bx * BOX, &tmV, bx * 64, g, row, &bars->kv_full[st]);
+        }
+      }
+      __syncwarp();
+      issued = j + 1;
+    }
+    wait_warp_drain(&bars->q_full, 0);
+    for (int j = max(0, issued - kStages); j < issued; ++j)
+      wait_warp_drain(&bars->kv_full[j % kStages], (j / kStages) & 1);
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    constexpr uint32_t ID_S = idesc_bf16_f32(128, kN, 0, 0);   // K and Q K-major
+    constexpr uint32_t ID_O = idesc_bf16_f32(128, kN, 1, 0);   // V^T MN-major, P K-major
+    const uint32_t sQ = smem_u32(smem + Q_OFF);
+    const uint32_t sK = smem_u32(smem + K_OFF);
+    const uint32_t sV = smem_u32(smem + V_OFF);
+    const uint32_t sP = smem_u32(smem + P_OFF);
+    auto issue_s = [&](int j) {
+      const uint32_t kb = sK + (j % kStages) * TILE;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t offk = (kk >> 2) * BOX + (kk & 3) * 32;
+        const uint32_t offq = (kk >> 2) * QBOX + (kk & 3) * 32;
+        mma_ss(tmem + S_COL + 16 * (j & 1), smem_desc_sw128(kb + offk, 16, 1024),
+               smem_desc_sw128(sQ + offq, 16, 1024), ID_S, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(&bars->s_full[j & 1]);
+    };
+    bool ok = wait_warp(&bars->q_full, 0, wc);
+    for (int j = 0; ok && j < 2 && j < n; ++j) {
+      if (!(ok = wait_warp(&bars->kv_full[j % kStages], (j / kStages) & 1, wc))) break;
+      tc_fence_after();
+      if (lane == 0) issue_s(j);
+      __syncwarp();
+    }
+    for (int j = 0; ok && j < n; ++j) {
+      const int st = j % kStages;
+      if (!(ok = wait_warp(&bars->p_full[j & 1], (j >> 1) & 1, wc))) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t vb = sV + st * TILE;
+        const uint32_t pb = sP + (j & 1) * 2 * PBOX;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)          // K = 128 keys, 16 per MMA
+          mma_ss(tmem + O_COL, smem_desc_sw128(vb + kk * 2048, BOX, 1024),
+                 smem_desc_sw128(pb + (kk >> 2) * PBOX + (kk & 3) * 32, 16, 1024), ID_O,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars->pv_done[j & 1]);
+        mma_commit(&bars->kv_empty[st]);
+      }
+      __syncwarp();
+      // S^T(j+2) over S buffer j&1, which the softmax of tile j has released
+      const int nx = j + 2;
+      if (nx < n) {
+        if (!(ok = wait_warp(&bars->kv_full[nx % kStages], (nx / kStages) & 1, wc))) break;
+        tc_fence_after();
+        if (lane == 0) issue_s(nx);
+        __syncwarp();
+      }
+    }
+    if (lane == 0) mma_commit(&bars->o_done);
+    __syncwarp();
+    wait_warp_drain(&bars->o_done, 0);
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int t = threadIdx.x;                  // key of the tile; head dim of O^T
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+    const float c2 = p.scale_log2;
+    float m_ref[kN], l_t[kN], lr_t[kN];
+#pragma unroll
+    for (int r = 0; r < kN; ++r) {
+      m_ref[r] = -INFINITY;
+      l_t[r] = 0.f;
+      lr_t[r] = 0.f;
+    }
+    int pv_waited = 0;                          // PV completions waited, in order
+    bool ok = true;
+    // Wait until PV(upto) has completed, taking every PV in order.  PV(k)
+    // signals pv_done[k & 1]; PV(k + 2) needs P(k + 2), which is written only
+    // after PV(k) was waited here, so a barrier never runs a phase ahead.
+    auto ensure_pv = [&](int upto) {
+      while (ok && pv_waited <= upto) {
+        ok = wait_warp(&bars->pv_done[pv_waited & 1], (pv_waited >> 1) & 1, wc);
+        ++pv_waited;
+      }
+    };
+    for (int j = 0; j < n; ++j) {
+      ok = wait_warp(&bars->s_full[j & 1], (j >> 1) & 1, wc);
+      float x[kN];
+      bool need = false;
+      if (ok) {
+        tc_fence_after();
+        uint32_t sv[kN];
+        tmem_ld16(lane_base + S_COL + 16 * (j & 1), sv);
+        tmem_wait_ld();
+        reg_fence16(sv);
+        const int key = kmin + 128 * j + t;
+#pragma unroll
+        for (int r = 0; r < kN; ++r) {
+          const int pos = rpos[r];
+          float xr = fmaf(__uint_as_float(sv[r]), c2, rslope[r] * (float)(key - pos));
+          if (r >= R || key >= k1 || key > pos || key < pos - W) xr = -INFINITY;
+          x[r] = xr;
+          need |= xr > m_ref[r] + kTau;         // also true on a row's first visible key
+        }
+      }
+      // every softmax warp learns whether any gave up, and whether any row
+      // must raise its reference
+      if (named_bar_any(1, 128, !ok)) {
+        ok = false;
+        break;
+      }
+      if (named_bar_any(1, 128, need)) {
+        // exact tile max per row: warp butterflies, then across the 4 warps
+#pragma unroll
+        for (int r = 0; r < kN; ++r) {
+          float mr = x[r];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, o));
+          if (lane == 0) red[warp * kN + r] = mr;
+        }
+        named_bar_sync(1, 128);
+        float alpha[kN];
+        bool any_raise = false;
+#pragma unroll
+        for (int r = 0; r < kN; ++r) {
+          const float tm = fmaxf(fmaxf(red[r], red[kN + r]), fmaxf(red[2 * kN + r], red[3 * kN + r]));
+          const float mn = fmaxf(m_ref[r], tm);
+          alpha[r] = (mn == -INFINITY || mn == m_ref[r]) ? 1.f : ex2_approx(m_ref[r] - mn);
+          any_raise |= mn != m_ref[r] && j > 0;
+          m_ref[r] = mn;
+          l_t[r] *= alpha[r];
+          lr_t[r] *= alpha[r];
+        }
+        named_bar_sync(1, 128);                 // red[] is reused by the next tile
+        if (any_raise) {                        // uniform over the block
+          ensure_pv(j - 1);                     // O^T holds PV(0..j-1) complete
+          uint32_t o[kN];
+          tmem_ld16(lane_base + O_COL, o);
+          tmem_wait_ld();
+          reg_fence16(o);
+#pragma unroll
+          for (int r = 0; r < kN; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
+          tmem_st16(lane_base + O_COL, o);
+          tmem_wait_st();
+        }
+      }
+      // P = 2^(x - m): bf16 to shared memory as the B operand of O^T (row r,
+      // key t: box t / 64, 16-byte chunk (t % 64) / 8 swizzled by r % 8)
+      ensure_pv(j - 2);                         // P buffer j&1 was read by PV(j-2)
+      uint8_t* pbuf = smem + P_OFF + (j & 1) * 2 * PBOX + (t >> 6) * PBOX;
+      const int kc = (t & 63) >> 3;
+      const int kb2 = (t & 7) * 2;
+#pragma unroll
+      for (int r = 0; r < kN; ++r) {
+        const float pr = m_ref[r] == -INFINITY ? 0.f : ex2_approx(x[r] - m_ref[r]);
+        const __nv_bfloat16 pb = __float2bfloat16_rn(pr);
+        l_t[r] += pr;
+        lr_t[r] += __bfloat162float(pb);
+        *reinterpret_cast<__nv_bfloat16*>(pbuf + (r >> 3) * 1024 + (r & 7) * 128 +
+                                           ((kc ^ (r & 7)) << 4) + kb2) = pb;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full[j & 1]);
+    }
+    // ------------------------------------------------- partial state
+    if (ok) ok = wait_warp(&bars->o_done, 0, wc);
+    if (named_bar_any(1, 128, !ok)) {
+      ok = false;
+    } else {
+      tc_fence_after();
+      uint32_t o[kN];
+      tmem_ld16(lane_base + O_COL, o);
+      tmem_wait_ld();
+      reg_fence16(o);
+#pragma unroll
+      for (int r = 0; r < kN; ++r)
+        if (r < R) po[r * D + t] = __uint_as_float(o[r]);
+      // l and l~ of each row: sums over the 128 key lanes (warp butterflies,
+      // then the four warps' partial sums through shared memory)
+      float mrow = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < kN; ++r) {
+        float a = l_t[r], c = lr_t[r];
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) {
+          a += __shfl_xor_sync(0xffffffffu, a, o2);
+          c += __shfl_xor_sync(0xffffffffu, c, o2);
+        }
+        if (lane == 0) {
+          red[warp * kN + r] = a;
+          red[(4 + warp) * kN + r] = c;
+        }
+        if (r == t) mrow = m_ref[r];
+      }
+      named_bar_sync(1, 128);
+      if (t < R) {
+        pml[3 * t] = mrow;
+        pml[3 * t + 1] = red[t] + red[kN + t] + red[2 * kN + t] + red[3 * kN + t];
+        pml[3 * t + 2] = red[4 * kN + t] + red[5 * kN + t] + red[6 * kN + t] + red[7 * kN + t];
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
+  }
+}
+
+int launch(const DecodeParams& p, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(decode_split_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SMEM_BYTES);
+  if (e != cudaSuccess) return (int)e;
+  CUtensorMap tq, tk, tv;
+  const long long rows = (long long)p.B * p.S_max;
+  int r = make_tmap_bf16_3d_box(&tq, p.q, 128, p.Hq, (long long)p.B * p.q_len, p.group, p.q_len);
+  if (!r) r = make_tmap_bf16_3d(&tk, p.k, 128, p.Hkv, rows, 128);
+  if (!r) r = make_tmap_bf16_3d(&tv, p.v, 128, p.Hkv, rows, 128);
+  if (r) return r;
+  const long long grid = (long long)p.B * p.Hkv * p.nsplit;
+  decode_split_tc_kernel<<<(unsigned)grid, kThreads, SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace tc
 
 // One warp per output row (query token, head): merge the chunks' partial
 // states, write O and LSE.
@@ -381,23 +760,26 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
   const int ns = (L + p.chunk - 1) / p.chunk;
   const long long u0 = ((long long)b * p.Hkv + g) * p.nsplit;
   float M = -INFINITY;
-  for (int s = lane; s < ns; s += 32) M = fmaxf(M, p.part_ml[((u0 + s) * p.R + r) * 2]);
+  for (int s = lane; s < ns; s += 32) M = fmaxf(M, p.part_ml[((u0 + s) * p.R + r) * 3]);
   M = warp_max(M);
   constexpr int PER = D / 32;
   float o[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) o[i] = 0.f;
-  float lsum = 0.f;
+  float lsum = 0.f, lrsum = 0.f;
   for (int s = 0; s < ns; ++s) {
-    const float ms = p.part_ml[((u0 + s) * p.R + r) * 2];
+    const float* ml = p.part_ml + ((u0 + s) * p.R + r) * 3;
+    const float ms = ml[0];
     if (ms == -INFINITY) continue;                // chunk with nothing visible
     const float wgt = ex2_approx(ms - M);
-    lsum = fmaf(wgt, p.part_ml[((u0 + s) * p.R + r) * 2 + 1], lsum);
+    lsum = fmaf(wgt, ml[1], lsum);
+    lrsum = fmaf(wgt, ml[2], lrsum);
     const float* src = p.part_o + ((u0 + s) * p.R + r) * D;
 #pragma unroll
     for (int i = 0; i < PER; ++i) o[i] = fmaf(wgt, src[lane + 32 * i], o[i]);
   }
-  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  // O is normalised by the weights its product used; LSE by the exact sum
+  const float inv = lrsum > 0.f ? 1.f / lrsum : 0.f;
   const long long orow = ((long long)tq * p.Hq + h) * D;
   if (p.o_f32) {
 #pragma unroll
@@ -430,7 +812,8 @@ int launch_split(const DecodeParams& p, cudaStream_t stream) {
 template <int D>
 int launch_d(const DecodeParams& p, cudaStream_t stream) {
   int r;
-  if (p.R <= 1) r = launch_split<D, 1>(p, stream);
+  if (D == 128) r = tc::launch(p, stream);
+  else if (p.R <= 1) r = launch_split<D, 1>(p, stream);
   else if (p.R <= 2) r = launch_split<D, 2>(p, stream);
   else if (p.R <= 4) r = launch_split<D, 4>(p, stream);
   else if (p.R <= 8) r = launch_split<D, 8>(p, stream);

@@ -87,7 +87,8 @@ struct DecodeParams {
   const int32_t* seqlens;      // [B] or nullptr (every cache holds S_max tokens)
   const float* alibi;          // [Hq] or nullptr
   float* part_o;               // [B, Hkv, nsplit, R, d] fp32: unnormalised partial O
-  float* part_ml;              // [B, Hkv, nsplit, R, 2] fp32: partial max (log2 units), sum
+  float* part_ml;              // [B, Hkv, nsplit, R, 3] fp32: partial max (log2 units),
+                               // sum of P (exact), sum of P as the PV product used it
   unsigned int* status;
   int B, Hq, Hkv, S_max, q_len, d, group, R;
   int chunk, nsplit;
@@ -101,10 +102,10 @@ struct DecodeParams {
 constexpr int kDecodeUnitsTarget = 8 * 152;
 constexpr int kDecodeMaxRows = 16;
 
-// Keys per decode block: the largest of 64, 128, ..., 4096 that still leaves
+// Keys per decode block: the largest of 128, 256, ..., 4096 that still leaves
 // kDecodeUnitsTarget blocks for B caches of S_max tokens.
 inline int decode_chunk(int B, int Hkv, int S_max) {
-  int c = 64;
+  int c = 128;
   while (c < 4096) {
     const long long n = (long long)B * Hkv * ((S_max + 2 * c - 1) / (2 * c));
     if (n < kDecodeUnitsTarget) break;

@@ -143,6 +143,6 @@ def test_decode_workspace_size(lib):
     n = fa.fa_decode_workspace_size(16, 32, 8, 32768, 1, 128)
     # 16 x 8 (sequence, kv head) pairs, chunks of 2048 keys -> 16 chunks; R = 4 rows
     units = 16 * 8 * 16
-    assert n == units * 4 * 128 * 4 + ((units * 4 * 2 * 4 + 255) // 256) * 256
+    assert n == units * 4 * 128 * 4 + ((units * 4 * 3 * 4 + 255) // 256) * 256
     assert fa.fa_decode_workspace_size(1, 3, 2, 64, 1, 64) == 0      # Hq % Hkv != 0
     assert fa.fa_decode_workspace_size(1, 32, 1, 64, 1, 64) == 0     # 32 rows
