@@ -54,16 +54,10 @@ struct DecCfg {
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + kStages * TILE;
   static constexpr int Q_OFF = V_OFF + kStages * TILE;           // fp32 [RM][D]
-  static constexpr int S_OFF = Q_OFF + RM * D * 4;               // fp32 [2][RM][64]
-  static constexpr int A_OFF = S_OFF + 2 * RM * kTileKeys * 4;   // fp32 [2][RM]
-  static constexpr int ROW_OFF = A_OFF + 2 * RM * 4;             // int pos[RM], float slope2[RM]
+  static constexpr int P_OFF = Q_OFF + RM * D * 4;               // fp32 [8 warps][RM][8]
+  static constexpr int ROW_OFF = P_OFF + 8 * RM * 8 * 4;          // int pos[RM], float slope2[RM]
   static constexpr int BAR_OFF = (ROW_OFF + 2 * RM * 4 + 15) / 16 * 16;
   static constexpr int SMEM_BYTES = BAR_OFF + 64 + 1024;
-  // PV ownership: thread = (column pair, row group)
-  static constexpr int NCP = D / 2;
-  static constexpr int NRG = kComputeThreads / NCP;
-  static constexpr int RPT = (RM + NRG - 1) / NRG;
-  static constexpr int RW = (RM + 7) / 8;                        // softmax rows per warp
 };
 
 struct DecBars {
@@ -78,12 +72,6 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-  return x;
-}
-
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
   return x;
 }
 
@@ -214,7 +202,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   const int kq = lane >> 2;
   const int cq = lane & 3;
   const int krow = 8 * warp + kq;
-  float* pw = reinterpret_cast<float*>(smem + C::S_OFF) + warp * RM * 8;   // P of the warp, [RM][8]
+  float* pw = reinterpret_cast<float*>(smem + C::P_OFF) + warp * RM * 8;   // P of the warp, [RM][8]
   float m_r[RM], l_r[RM];
   uint64_t o2[RM][CPL / 2];
 #pragma unroll

@@ -56,23 +56,24 @@ __device__ __forceinline__ void load_row(const __nv_bfloat16* x, int H, long lon
   v[1] = __uint_as_float(raw.x & 0xFFFF0000u);
   v[2] = __uint_as_float(raw.y << 16);
   v[3] = __uint_as_float(raw.y & 0xFFFF0000u);
-  if (!TRANSFORM) return;
+  if constexpr (TRANSFORM) {
 #pragma unroll
-  for (int e = 0; e < 4; ++e) v[e] *= sg[e];
-  // stride 1: (0,1), (2,3);  stride 2: (0,2), (1,3)
-  float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
-  v[0] = a0 + a2;
-  v[1] = a1 + a3;
-  v[2] = a0 - a2;
-  v[3] = a1 - a3;
-  // strides 4 .. 64: column c = 4 lane + e pairs with c ^ stride, in lane ^ (stride / 4)
+    for (int e = 0; e < 4; ++e) v[e] *= sg[e];
+    // stride 1: (0,1), (2,3);  stride 2: (0,2), (1,3)
+    float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
+    v[0] = a0 + a2;
+    v[1] = a1 + a3;
+    v[2] = a0 - a2;
+    v[3] = a1 - a3;
+    // strides 4 .. 64: column c = 4 lane + e pairs with c ^ stride, in lane ^ (stride / 4)
 #pragma unroll
-  for (int sl = 1; sl < 32; sl <<= 1) {
-    const bool upper = (lane & sl) != 0;          // this lane holds the (a, b) pair's b
+    for (int sl = 1; sl < 32; sl <<= 1) {
+      const bool upper = (lane & sl) != 0;          // this lane holds the (a, b) pair's b
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float o = __shfl_xor_sync(0xffffffffu, v[e], sl);
-      v[e] = upper ? o - v[e] : v[e] + o;
+      for (int e = 0; e < 4; ++e) {
+        const float o = __shfl_xor_sync(0xffffffffu, v[e], sl);
+        v[e] = upper ? o - v[e] : v[e] + o;
+      }
     }
   }
 }
