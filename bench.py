@@ -62,6 +62,9 @@ def parse():
                     help="time the FP8 forward (quantize + e4m3 attention) on the workload")
     ap.add_argument("--deterministic", action="store_true",
                     help="time the deterministic backward (dQ by its own kernel, no atomics)")
+    ap.add_argument("--record-traffic", metavar="NCU_CSV",
+                    help="do not run: store the DRAM bytes per launch from an ncu --csv log of "
+                         "this workload / mode in profiles/ncu_dram_traffic.json and exit")
     return ap.parse_args()
 
 
@@ -137,6 +140,91 @@ def ncu_traffic(workload: str, kernel: str):
         return rec["bytes_per_launch"]
     except Exception:
         return None
+
+
+# ncu kernel-name fragment -> (per-kernel key, the source files it is built from).
+# The decode call (split + combine) and the FP8 quantize call (Q, K, then V)
+# launch several kernels; their figures are summed per call, a call being
+# counted by the launches of its last kernel (CALL_LAST).
+_COMMON_SOURCES = ["fa_ptx.cuh", "fa_internal.h", "fa_host_util.cu"]
+KERNEL_SOURCES = [
+    ("fwd_bf16_kernel", "fwd", "fa_fwd_bf16.cu"),
+    ("bwd_preprocess_kernel", "bwd_preprocess", "fa_bwd_bf16.cu"),
+    ("bwd_dkdv_kernel", "bwd_dkdv", "fa_bwd_bf16.cu"),
+    ("bwd_dq_convert_kernel", "bwd_dq_convert", "fa_bwd_bf16.cu"),
+    ("bwd_dq_kernel", "bwd_dq", "fa_bwd_dq_bf16.cu"),
+    ("fwd_fp8_kernel", "fwd_fp8", "fa_fwd_fp8.cu"),
+    ("quant_", "fp8_quantize", "fa_fp8_quant.cu"),
+    ("decode_", "decode", "fa_decode_bf16.cu"),
+]
+CALL_LAST = {"decode": "combine", "fp8_quantize": "quant_v"}
+_BYTE_UNITS = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12}
+_TIME_UNITS = {"ns": 1, "us": 1e3, "usecond": 1e3, "ms": 1e6, "msecond": 1e6, "nsecond": 1}
+
+
+def traffic_key(args) -> str:
+    return args.workload + (" fp8" if args.fp8 else "") + (" deterministic" if args.deterministic else "")
+
+
+def record_traffic(csv_path: str, key: str) -> dict:
+    """Per-kernel DRAM bytes per launch from an `ncu --csv` metrics log.
+
+    Launches of one kernel are averaged; the decode call's split and combine
+    kernels (and the FP8 quantizer's three) are summed per call.  Each
+    entry carries a hash of every source the kernel is built from, so that
+    ncu_traffic() drops it once the kernel changes."""
+    import csv
+    rows = [r for r in csv.reader(open(csv_path)) if r]
+    hdr = next(i for i, r in enumerate(rows) if "Metric Name" in r)
+    h = rows[hdr]
+    col = {n: h.index(n) for n in ("ID", "Kernel Name", "Metric Name", "Metric Unit", "Metric Value")}
+    launches = {}
+    for r in rows[hdr + 1:]:
+        if len(r) != len(h):
+            continue
+        name = r[col["Kernel Name"]]
+        match = next((k for k in KERNEL_SOURCES if k[0] in name), None)
+        if match is None:
+            continue
+        lid = r[col["ID"]]
+        rec = launches.setdefault(lid, {"kernel": match[1], "source": match[2], "name": name})
+        unit, metric = r[col["Metric Unit"]], r[col["Metric Name"]]
+        try:
+            val = float(r[col["Metric Value"]].replace(",", ""))
+        except ValueError:           # a metric this kernel does not report ("n/a")
+            continue
+        if metric in ("dram__bytes_read.sum", "dram__bytes_write.sum", "lts__t_bytes.sum"):
+            val *= _BYTE_UNITS.get(unit, 1)
+        elif metric == "gpu__time_duration.sum":
+            val *= _TIME_UNITS.get(unit, 1)
+        rec[metric] = val
+    per = {}
+    for rec in launches.values():
+        per.setdefault(rec["kernel"], []).append(rec)
+    out = {}
+    for kern, recs in per.items():
+        last = CALL_LAST.get(kern)
+        calls = len(recs) if last is None else max(1, sum(last in r["name"] for r in recs))
+        tot = lambda m: sum(r.get(m, 0.0) for r in recs) / calls
+        rd, wr = tot("dram__bytes_read.sum"), tot("dram__bytes_write.sum")
+        srcs = [recs[0]["source"]] + _COMMON_SOURCES
+        out[kern] = {"sources_sha256_16": {n: source_hash(n) for n in srcs},
+                     "dram_bytes_read": int(rd), "dram_bytes_write": int(wr),
+                     "bytes_per_launch": int(rd + wr),
+                     "gpu_time_ns_under_ncu": int(tot("gpu__time_duration.sum")),
+                     "launches_averaged": calls}
+        if any("lts__t_bytes.sum" in r for r in recs):
+            out[kern]["lts_bytes"] = int(tot("lts__t_bytes.sum"))
+    try:
+        with open(TRAFFIC_FILE) as f:
+            table = json.load(f)
+    except Exception:
+        table = {}
+    table[key] = out
+    with open(TRAFFIC_FILE, "w") as f:
+        json.dump(table, f, indent=1)
+        f.write("\n")
+    return out
 
 
 class ClockSampler:
@@ -728,6 +816,9 @@ def run_reference(args, world, rank):
 
 def main():
     args = parse()
+    if args.record_traffic:
+        print(json.dumps({traffic_key(args): record_traffic(args.record_traffic, traffic_key(args))}))
+        return
     world, rank, local = dist_info()
     if args.impl == "reference":
         run_reference(args, world, rank)

@@ -99,46 +99,68 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }
 
 // ----------------------------------------------------------------- preprocess
-// One warp per (token, query head): D = dO . O in fp32, and the dQ
-// accumulator row zeroed (not in the deterministic backward, which has no
-// accumulator).
+// D = dO . O in fp32 per (token, query head), and the dQ accumulator row
+// zeroed (not in the deterministic backward, which has no accumulator).
+// A thread takes 8 consecutive elements of a row (16-byte loads), D / 8
+// threads share a row, and each thread handles kPreRows rows, their loads
+// issued before any arithmetic so that enough bytes are in flight to stream
+// at HBM speed.
+constexpr int kPreRows = 2;
+
+template <int D>
+__device__ __forceinline__ void load8_f32(const void* base, bool f32, long long off, float (&x)[8]) {
+  if (f32) {
+    const float4* q = reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
+    const float4 a = q[0], b = q[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  } else {
+    const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + off);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const AttnParams p) {
-  const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (w >= p.T * p.Hq) return;
-  const long long t = w / p.Hq;
-  const int h = (int)(w - t * p.Hq);
-  const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(p.dO) + (t * p.Hq + h) * D;
-  constexpr int PER = D / 32;   // elements per lane: 2 or 4
-  float o_v[PER], g_v[PER];
-  if (PER == 4) {
-    const uint2 bb = reinterpret_cast<const uint2*>(g)[lane];
-    const float2 y0 = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(&bb)[0]);
-    const float2 y1 = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(&bb)[1]);
-    g_v[0] = y0.x; g_v[1] = y0.y; g_v[2 % PER] = y1.x; g_v[3 % PER] = y1.y;
-  } else {
-    const float2 y = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(g)[lane]);
-    g_v[0] = y.x; g_v[1 % PER] = y.y;
+  constexpr int G = D / 8;                       // threads per row
+  constexpr int RPB = 256 / G;                   // rows per block and pass
+  const int c8 = threadIdx.x % G;
+  const long long rows = p.T * p.Hq;
+  float o_v[kPreRows][8], g_v[kPreRows][8];
+  long long r[kPreRows];
+#pragma unroll
+  for (int i = 0; i < kPreRows; ++i) {
+    r[i] = ((long long)blockIdx.x * kPreRows + i) * RPB + threadIdx.x / G;
+    if (r[i] < rows) {
+      load8_f32<D>(p.dO, false, r[i] * D + 8 * c8, g_v[i]);
+      load8_f32<D>(p.o, p.o_f32 != 0, r[i] * D + 8 * c8, o_v[i]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) g_v[i][e] = o_v[i][e] = 0.f;
+    }
   }
-  if (p.o_f32) {
-    const float* o = static_cast<const float*>(p.o) + (t * p.Hq + h) * D + lane * PER;
 #pragma unroll
-    for (int i = 0; i < PER; ++i) o_v[i] = o[i];
-  } else {
-    const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(p.o) + (t * p.Hq + h) * D + lane * PER;
+  for (int i = 0; i < kPreRows; ++i) {
+    float acc = 0.f;
 #pragma unroll
-    for (int i = 0; i < PER; ++i) o_v[i] = __bfloat162float(o[i]);
+    for (int e = 0; e < 8; ++e) acc = fmaf(o_v[i][e], g_v[i][e], acc);
+#pragma unroll
+    for (int s = G / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (r[i] >= rows) continue;
+    const long long t = r[i] / p.Hq;
+    const int h = (int)(r[i] - t * p.Hq);
+    if (c8 == 0) p.D[(long long)h * p.T + t] = acc;
+    if (!p.deterministic) {          // the deterministic backward's dQ kernel has no accumulator
+      float4* z = reinterpret_cast<float4*>(p.dq_acc + ((long long)h * p.T + t) * D + 8 * c8);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
-  float acc = 0.f;
-#pragma unroll
-  for (int i = 0; i < PER; ++i) acc = fmaf(o_v[i], g_v[i], acc);
-#pragma unroll
-  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (lane == 0) p.D[(long long)h * p.T + t] = acc;
-  if (p.deterministic) return;           // dQ has its own kernel: no accumulator
-  float4* z = reinterpret_cast<float4*>(p.dq_acc + ((long long)h * p.T + t) * D);
-  if (lane < D / 4) z[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ----------------------------------------------------------------- dq convert
@@ -609,7 +631,8 @@ template <int D>
 int launch_stages(const AttnParams& p, cudaStream_t stream, int stage) {
   const long long rows = p.T * p.Hq;
   if (stage < 0 || stage == 0) {
-    bwd_preprocess_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
+    const long long per_block = (long long)kPreRows * (256 / (D / 8));
+    bwd_preprocess_kernel<D><<<(unsigned)((rows + per_block - 1) / per_block), 256, 0, stream>>>(p);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return (int)e;
   }
