@@ -10,6 +10,9 @@ error, no timed-out wait) and prints the rates it measured:
                   alone and together.
 * reduce_rate.cu  L2 throughput of cp.reduce.async.bulk .add.f32 into an
                   accumulator larger than L2 and into one that fits.
+* alu_rate.cu     per-SM rates of the forward softmax's per-score
+                  instructions (ex2, cvt to bf16x2, prmt, packed add) and of
+                  its whole per-pair body with either bf16 packing.
 
 All operands are zero and every wait is bounded; nothing here faults or hangs.
 """
@@ -40,8 +43,8 @@ def _build_and_run(name, tmp_path):
     return out
 
 
-@pytest.mark.parametrize("name", ["mma_rate", "mma_mix", "reduce_rate"])
+@pytest.mark.parametrize("name", ["mma_rate", "mma_mix", "reduce_rate", "alu_rate"])
 def test_probe(name, tmp_path):
     out = _build_and_run(name, tmp_path)
-    rates = [float(x) for x in re.findall(r"([\d.]+) T[BF]", out)]
+    rates = [float(a or b) for a, b in re.findall(r"([\d.]+) T[BF]|rate=([\d.]+)", out)]
     assert rates and min(rates) > 0
