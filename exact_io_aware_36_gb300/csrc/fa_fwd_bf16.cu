@@ -7,11 +7,13 @@
 // row), Key design 4 (FA3-style asynchrony: producer and consumer roles).
 //
 // GB300 mapping (one CTA per SM, 320 threads, 2 query tiles of 128 rows):
-//   warp 9     TMA producer: Q0/Q1 once, then K_j and V_j into two rings
-//              (128-byte swizzle) with their own full/empty mbarriers: a K
-//              slot is released once both S MMAs of its tile are done, a V
-//              slot once both PV MMAs are, so the next K load never waits
-//              for the slower V release.
+//   warp 9     TMA producer: Q0/Q1 once, then per step j one slot holding
+//              K_j and V_{j-1} (128-byte swizzle), with one full and one
+//              empty mbarrier per slot.  Step j's products are S_t(j), which
+//              reads K_j, and PV_t(j-1), which reads V_{j-1}; both are done
+//              when the slot is released, so pairing the two tiles this way
+//              holds neither back, and the MMA warp has one wait and one
+//              release per step.
 //   warp 8     MMA issuer (one lane): S_t = Q_t K_j^T into TMEM (both
 //              operands K-major in shared memory), then O_t += P_t V_j with
 //              P_t read from TMEM and V_j MN-major in shared memory.
@@ -49,12 +51,11 @@ struct FwdCfg {
   static constexpr int NB = D / 64;                 // 64-column boxes per row
   static constexpr int BOX_BYTES = 128 * 64 * 2;    // one 128 x 64 bf16 box
   static constexpr int TILE_BYTES = NB * BOX_BYTES; // one 128 x D tile
-  static constexpr int KS = D == 128 ? 3 : 6;      // K ring stages
-  static constexpr int VS = D == 128 ? 2 : 4;      // V ring stages
+  static constexpr int NS = D == 128 ? 2 : 5;      // slots (K_j, V_{j-1})
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + 2 * TILE_BYTES;
-  static constexpr int V_OFF = K_OFF + KS * TILE_BYTES;
-  static constexpr int BAR_OFF = V_OFF + VS * TILE_BYTES;
+  static constexpr int V_OFF = K_OFF + NS * TILE_BYTES;
+  static constexpr int BAR_OFF = V_OFF + NS * TILE_BYTES;
   static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
   static constexpr uint32_t S_COL0 = 0, S_COL1 = 128;
   static constexpr uint32_t O_COL0 = 256, O_COL1 = 256 + D;
@@ -62,7 +63,7 @@ struct FwdCfg {
 
 struct FwdBars {
   uint64_t q_full;
-  uint64_t k_full[8], k_empty[8], v_full[8], v_empty[8];
+  uint64_t kv_full[8], kv_empty[8];
   uint64_t s_full[2], p_full[2];
   uint64_t o_done;
   uint32_t tmem_base;
@@ -146,10 +147,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     mbar_init(&bars->q_full, 1);
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
-      mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
-      mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], 1);
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
@@ -185,37 +184,30 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                       (int)(seq0 + m0 + 128 * t), &bars->q_full);
     }
     __syncwarp();
-    int issued_k = 0, issued_v = 0;   // tiles whose loads were issued
-    for (int j = 0; j < nkv_max; ++j) {       // j: step index; kvj(j): kv tile
-      const int sk = j % C::KS;
-      if (!wait_warp(&bars->k_empty[sk], ((j / C::KS) & 1) ^ 1, wc)) break;
+    int issued = 0;                   // slots whose loads were issued
+    for (int j = 0; j <= nkv_max; ++j) {      // j: step; its slot holds K_j and V_{j-1}
+      const int sl = j % C::NS;
+      if (!wait_warp(&bars->kv_empty[sl], ((j / C::NS) & 1) ^ 1, wc)) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->k_full[sk], C::TILE_BYTES);
+        const bool has_k = j < nkv_max, has_v = j >= 1;
+        mbar_arrive_expect_tx(&bars->kv_full[sl], (has_k + has_v) * C::TILE_BYTES);
 #pragma unroll
-        for (int bx = 0; bx < C::NB; ++bx)
-          tma_load_3d(smem + C::K_OFF + sk * C::TILE_BYTES + bx * C::BOX_BYTES, &tmK, bx * 64, kvh,
-                      (int)(seq0 + 128 * kvj(j)), &bars->k_full[sk]);
+        for (int bx = 0; bx < C::NB; ++bx) {
+          if (has_k)
+            tma_load_3d(smem + C::K_OFF + sl * C::TILE_BYTES + bx * C::BOX_BYTES, &tmK, bx * 64, kvh,
+                        (int)(seq0 + 128 * kvj(j)), &bars->kv_full[sl]);
+          if (has_v)
+            tma_load_3d(smem + C::V_OFF + sl * C::TILE_BYTES + bx * C::BOX_BYTES, &tmV, bx * 64, kvh,
+                        (int)(seq0 + 128 * kvj(j - 1)), &bars->kv_full[sl]);
+        }
       }
       __syncwarp();
-      issued_k = j + 1;
-      const int sv = j % C::VS;
-      if (!wait_warp(&bars->v_empty[sv], ((j / C::VS) & 1) ^ 1, wc)) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->v_full[sv], C::TILE_BYTES);
-#pragma unroll
-        for (int bx = 0; bx < C::NB; ++bx)
-          tma_load_3d(smem + C::V_OFF + sv * C::TILE_BYTES + bx * C::BOX_BYTES, &tmV, bx * 64, kvh,
-                      (int)(seq0 + 128 * kvj(j)), &bars->v_full[sv]);
-      }
-      __syncwarp();
-      issued_v = j + 1;
+      issued = j + 1;
     }
     // Loads in flight must land before this CTA's shared memory goes away.
     wait_warp_drain(&bars->q_full, 0);
-    for (int j = max(0, issued_k - C::KS); j < issued_k; ++j)
-      wait_warp_drain(&bars->k_full[j % C::KS], (j / C::KS) & 1);
-    for (int j = max(0, issued_v - C::VS); j < issued_v; ++j)
-      wait_warp_drain(&bars->v_full[j % C::VS], (j / C::VS) & 1);
+    for (int j = max(0, issued - C::NS); j < issued; ++j)
+      wait_warp_drain(&bars->kv_full[j % C::NS], (j / C::NS) & 1);
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);
@@ -227,18 +219,17 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const uint32_t colO[2] = {C::O_COL0, C::O_COL1};
     bool ok = wait_warp(&bars->q_full, 0, wc);
     for (int j = 0; ok && j <= nkv_max; ++j) {
-      const int sj = j % C::KS;                       // K_j
-      const int sp = (j + C::VS - 1) % C::VS;         // V_{j-1}
-      if (j < nkv_max && !(ok = wait_warp(&bars->k_full[sj], (j / C::KS) & 1, wc))) break;
-      if (j >= 1 && !(ok = wait_warp(&bars->v_full[sp], ((j - 1) / C::VS) & 1, wc))) break;
-      tc_fence_after();
+      const int sl = j % C::NS;                       // K_j and V_{j-1}
+      // TMA data needs no tcgen05 fence: the MMAs read it once the
+      // transaction count of the slot's barrier has completed.
+      if (!(ok = wait_warp(&bars->kv_full[sl], (j / C::NS) & 1, wc))) break;
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (j >= 1 && j - 1 >= k0[t] && j - 1 < k0[t] + nkv[t]) {
           if (!(ok = wait_warp(&bars->p_full[t], (j - 1 - k0[t]) & 1, wc))) break;
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t vbase = sV + sp * C::TILE_BYTES;
+            const uint32_t vbase = sV + sl * C::TILE_BYTES;
 #pragma unroll
             for (int kk = 0; kk < 128 / 16; ++kk) {
               const uint64_t bdesc = smem_desc_sw128(vbase + kk * 2048, C::BOX_BYTES, 1024);
@@ -251,7 +242,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (j >= k0[t] && j < k0[t] + nkv[t]) {
           if (lane == 0) {
             const uint32_t qbase = sQ + t * C::TILE_BYTES;
-            const uint32_t kbase = sK + sj * C::TILE_BYTES;
+            const uint32_t kbase = sK + sl * C::TILE_BYTES;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
@@ -265,10 +256,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
       }
       if (!ok) break;
-      if (lane == 0) {
-        if (j < nkv_max) mma_commit(&bars->k_empty[sj]);
-        if (j >= 1) mma_commit(&bars->v_empty[sp]);
-      }
+      if (lane == 0) mma_commit(&bars->kv_empty[sl]);
       __syncwarp();
     }
     if (lane == 0) mma_commit(&bars->o_done);
