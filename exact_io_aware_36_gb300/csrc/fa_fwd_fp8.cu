@@ -22,7 +22,9 @@
 //     K-major operands from shared memory;
 //   - P8 written by the softmax warps to shared memory (128 rows x 128 keys,
 //     swizzled) instead of TMEM, as the A operand of the PV product;
-//   - 4 K and 4 V stages (16 KB each).
+//   - 4 slots of 16 KB K and 16 KB V: slot j holds K_j and V_{j-1}, the
+//     operands of step j's products S_t(j) and PV_t(j-1), under one full and
+//     one empty barrier (one wait and one release per step for the MMA warp).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -43,11 +45,11 @@ constexpr int kD = 128;
 
 struct Cfg {
   static constexpr int TILE = 128 * 128;           // 128 rows x 128 bytes
-  static constexpr int KS = 4, VS = 4;
+  static constexpr int NS = 4;                     // slots (K_j, V_{j-1})
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + 2 * TILE;
-  static constexpr int V_OFF = K_OFF + KS * TILE;
-  static constexpr int P_OFF = V_OFF + VS * TILE;
+  static constexpr int V_OFF = K_OFF + NS * TILE;
+  static constexpr int P_OFF = V_OFF + NS * TILE;
   static constexpr int BAR_OFF = P_OFF + 2 * TILE;
   static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
   static constexpr uint32_t S_COL0 = 0, S_COL1 = 128;
@@ -56,7 +58,7 @@ struct Cfg {
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[8], k_empty[8], v_full[8], v_empty[8];
+  uint64_t kv_full[8], kv_empty[8];
   uint64_t s_full[2], p_full[2];
   uint64_t o_done;
   uint32_t tmem_base;
@@ -164,10 +166,8 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     mbar_init(&bars->q_full, 1);
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
-      mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
-      mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], 1);
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
@@ -199,32 +199,26 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         tma_load_3d(smem + C::Q_OFF + t * C::TILE, &tmQ, 0, h, (int)(seq0 + m0 + 128 * t), &bars->q_full);
     }
     __syncwarp();
-    int issued_k = 0, issued_v = 0;
-    for (int j = 0; j < nkv_max; ++j) {
-      const int sk = j % C::KS;
-      if (!wait_warp(&bars->k_empty[sk], ((j / C::KS) & 1) ^ 1, wc)) break;
+    int issued = 0;
+    for (int j = 0; j <= nkv_max; ++j) {      // step j: its slot holds K_j and V_{j-1}
+      const int sl = j % C::NS;
+      if (!wait_warp(&bars->kv_empty[sl], ((j / C::NS) & 1) ^ 1, wc)) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->k_full[sk], C::TILE);
-        tma_load_3d(smem + C::K_OFF + sk * C::TILE, &tmK, 0, kvh, (int)(seq0 + 128 * kvj(j)), &bars->k_full[sk]);
-      }
-      __syncwarp();
-      issued_k = j + 1;
-      const int sv = j % C::VS;
-      if (!wait_warp(&bars->v_empty[sv], ((j / C::VS) & 1) ^ 1, wc)) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->v_full[sv], C::TILE);
+        const bool has_k = j < nkv_max, has_v = j >= 1;
+        mbar_arrive_expect_tx(&bars->kv_full[sl], (has_k + has_v) * C::TILE);
+        if (has_k)
+          tma_load_3d(smem + C::K_OFF + sl * C::TILE, &tmK, 0, kvh, (int)(seq0 + 128 * kvj(j)), &bars->kv_full[sl]);
         // transposed V codes: x = key column of block (b, kvj), always a multiple of 128
-        tma_load_3d(smem + C::V_OFF + sv * C::TILE, &tmV, (int)(((long long)b * p.nblk + kvj(j)) * 128), 0,
-                    kvh, &bars->v_full[sv]);
+        if (has_v)
+          tma_load_3d(smem + C::V_OFF + sl * C::TILE, &tmV, (int)(((long long)b * p.nblk + kvj(j - 1)) * 128), 0,
+                      kvh, &bars->kv_full[sl]);
       }
       __syncwarp();
-      issued_v = j + 1;
+      issued = j + 1;
     }
     wait_warp_drain(&bars->q_full, 0);
-    for (int j = max(0, issued_k - C::KS); j < issued_k; ++j)
-      wait_warp_drain(&bars->k_full[j % C::KS], (j / C::KS) & 1);
-    for (int j = max(0, issued_v - C::VS); j < issued_v; ++j)
-      wait_warp_drain(&bars->v_full[j % C::VS], (j / C::VS) & 1);
+    for (int j = max(0, issued - C::NS); j < issued; ++j)
+      wait_warp_drain(&bars->kv_full[j % C::NS], (j / C::NS) & 1);
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     constexpr uint32_t IDESC = idesc_e4m3_f32(128, 128);   // S and O: M = N = 128
@@ -236,11 +230,10 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const uint32_t colO[2] = {C::O_COL0, C::O_COL1};
     bool ok = wait_warp(&bars->q_full, 0, wc);
     for (int j = 0; ok && j <= nkv_max; ++j) {
-      const int sj = j % C::KS;
-      const int sp = (j + C::VS - 1) % C::VS;          // V_{j-1}
-      if (j < nkv_max && !(ok = wait_warp(&bars->k_full[sj], (j / C::KS) & 1, wc))) break;
-      if (j >= 1 && !(ok = wait_warp(&bars->v_full[sp], ((j - 1) / C::VS) & 1, wc))) break;
-      tc_fence_after();
+      const int sl = j % C::NS;                        // K_j and V_{j-1}
+      // TMA data needs no tcgen05 fence: the MMAs read it once the
+      // transaction count of the slot's barrier has completed.
+      if (!(ok = wait_warp(&bars->kv_full[sl], (j / C::NS) & 1, wc))) break;
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (j >= 1 && j - 1 >= k0[t] && j - 1 < k0[t] + nkv[t]) {
@@ -250,7 +243,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)             // 32 keys per MMA
               mma_ss_f8(tmem + colO[t], smem_desc_sw128(sP + t * C::TILE + kk * 32, 16, 1024),
-                        smem_desc_sw128(sV + sp * C::TILE + kk * 32, 16, 1024), IDESC,
+                        smem_desc_sw128(sV + sl * C::TILE + kk * 32, 16, 1024), IDESC,
                         (j - 1 > k0[t] || kk > 0) ? 1u : 0u);
           }
           __syncwarp();
@@ -260,17 +253,14 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)             // 32 head dims per MMA
               mma_ss_f8(tmem + colS[t], smem_desc_sw128(sQ + t * C::TILE + kk * 32, 16, 1024),
-                        smem_desc_sw128(sK + sj * C::TILE + kk * 32, 16, 1024), IDESC, kk > 0 ? 1u : 0u);
+                        smem_desc_sw128(sK + sl * C::TILE + kk * 32, 16, 1024), IDESC, kk > 0 ? 1u : 0u);
             mma_commit(&bars->s_full[t]);
           }
           __syncwarp();
         }
       }
       if (!ok) break;
-      if (lane == 0) {
-        if (j < nkv_max) mma_commit(&bars->k_empty[sj]);
-        if (j >= 1) mma_commit(&bars->v_empty[sp]);
-      }
+      if (lane == 0) mma_commit(&bars->kv_empty[sl]);
       __syncwarp();
     }
     if (lane == 0) mma_commit(&bars->o_done);
