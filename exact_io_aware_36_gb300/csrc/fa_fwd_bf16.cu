@@ -217,9 +217,15 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const uint32_t sV = smem_u32(smem + C::V_OFF);
     const uint32_t colS[2] = {C::S_COL0, C::S_COL1};
     const uint32_t colO[2] = {C::O_COL0, C::O_COL1};
+    // Base descriptors, built once; each MMA's operand is an offset from them.
+    const uint64_t qdesc[2] = {smem_desc_sw128(sQ, 16, 1024), smem_desc_sw128(sQ + C::TILE_BYTES, 16, 1024)};
+    const uint64_t kdesc0 = smem_desc_sw128(sK, 16, 1024);
+    const uint64_t vdesc0 = smem_desc_sw128(sV, C::BOX_BYTES, 1024);
     bool ok = wait_warp(&bars->q_full, 0, wc);
     for (int j = 0; ok && j <= nkv_max; ++j) {
       const int sl = j % C::NS;                       // K_j and V_{j-1}
+      const uint64_t kdesc = desc_add(kdesc0, sl * C::TILE_BYTES);
+      const uint64_t vdesc = desc_add(vdesc0, sl * C::TILE_BYTES);
       // TMA data needs no tcgen05 fence: the MMAs read it once the
       // transaction count of the slot's barrier has completed.
       if (!(ok = wait_warp(&bars->kv_full[sl], (j / C::NS) & 1, wc))) break;
@@ -229,26 +235,19 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           if (!(ok = wait_warp(&bars->p_full[t], (j - 1 - k0[t]) & 1, wc))) break;
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t vbase = sV + sl * C::TILE_BYTES;
 #pragma unroll
-            for (int kk = 0; kk < 128 / 16; ++kk) {
-              const uint64_t bdesc = smem_desc_sw128(vbase + kk * 2048, C::BOX_BYTES, 1024);
-              mma_ts(tmem + colO[t], tmem + colS[t] + kk * 8, bdesc, IDESC_O,
+            for (int kk = 0; kk < 128 / 16; ++kk)
+              mma_ts(tmem + colO[t], tmem + colS[t] + kk * 8, desc_add(vdesc, kk * 2048), IDESC_O,
                      (j - 1 > k0[t] || kk > 0) ? 1u : 0u);
-            }
           }
           __syncwarp();
         }
         if (j >= k0[t] && j < k0[t] + nkv[t]) {
           if (lane == 0) {
-            const uint32_t qbase = sQ + t * C::TILE_BYTES;
-            const uint32_t kbase = sK + sl * C::TILE_BYTES;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-              const uint64_t adesc = smem_desc_sw128(qbase + off, 16, 1024);
-              const uint64_t bdesc = smem_desc_sw128(kbase + off, 16, 1024);
-              mma_ss(tmem + colS[t], adesc, bdesc, IDESC_S, kk > 0 ? 1u : 0u);
+              mma_ss(tmem + colS[t], desc_add(qdesc[t], off), desc_add(kdesc, off), IDESC_S, kk > 0 ? 1u : 0u);
             }
             mma_commit(&bars->s_full[t]);
           }

@@ -294,6 +294,15 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
       :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// The descriptor of an operand `bytes` further on in shared memory: the start
+// address sits in the low 14 bits in 16-byte units, and shared addresses stay
+// below 256 KB, so adding to the whole descriptor cannot carry out of the
+// field.  Cheaper than rebuilding the descriptor per MMA, which matters: the
+// issuing thread only stays ahead of the tensor pipe by a couple of MMAs.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
+  return desc + (uint64_t)(bytes >> 4);
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
