@@ -324,32 +324,29 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const uint32_t sQ = smem_u32(smem + C::Q_OFF);
     const uint32_t sdO = smem_u32(smem + C::DO_OFF);
     const uint32_t sdS = smem_u32(smem + C::DS_OFF);
+    // Base descriptors, built once; each MMA's operand is an offset from them.
+    const uint64_t kdesc = smem_desc_sw128(sK, 16, 1024), vdesc = smem_desc_sw128(sV, 16, 1024);
+    const uint64_t qdesc0 = smem_desc_sw128(sQ, 16, 1024), odesc0 = smem_desc_sw128(sdO, 16, 1024);
+    const uint64_t qmn0 = smem_desc_sw128(sQ, C::Q_BOX, 1024), omn0 = smem_desc_sw128(sdO, C::Q_BOX, 1024);
+    const uint64_t kmn = smem_desc_sw128(sK, C::KV_BOX, 1024), dsmn0 = smem_desc_sw128(sdS, C::Q_BOX, 1024);
 
     // S^T(i) into buffer i%2 and dP^T(i) into buffer i%2 (dP waits for the
     // dQ drain of step i-2, which used the same columns).
     auto issue_s = [&](int i) {
-      const int st = i % kQStages;
-      const uint32_t qb = sQ + st * C::Q_TILE;
+      const uint64_t qd = desc_add(qdesc0, (i % kQStages) * C::Q_TILE);
       const uint32_t dcol = C::SB_COL0 + 64 * (i & 1);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t offk = (kk >> 2) * C::KV_BOX + (kk & 3) * 32;
-        const uint32_t offq = (kk >> 2) * C::Q_BOX + (kk & 3) * 32;
-        mma_ss(tmem + dcol, smem_desc_sw128(sK + offk, 16, 1024), smem_desc_sw128(qb + offq, 16, 1024),
-               ID_S, kk > 0 ? 1u : 0u);
-      }
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss(tmem + dcol, desc_add(kdesc, (kk >> 2) * C::KV_BOX + (kk & 3) * 32),
+               desc_add(qd, (kk >> 2) * C::Q_BOX + (kk & 3) * 32), ID_S, kk > 0 ? 1u : 0u);
     };
     auto issue_dp = [&](int i) {
-      const int st = i % kQStages;
-      const uint32_t ob = sdO + st * C::Q_TILE;
+      const uint64_t od = desc_add(odesc0, (i % kQStages) * C::Q_TILE);
       const uint32_t dcol = C::PB_COL0 + 64 * (i & 1);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t offk = (kk >> 2) * C::KV_BOX + (kk & 3) * 32;
-        const uint32_t offq = (kk >> 2) * C::Q_BOX + (kk & 3) * 32;
-        mma_ss(tmem + dcol, smem_desc_sw128(sV + offk, 16, 1024), smem_desc_sw128(ob + offq, 16, 1024),
-               ID_S, kk > 0 ? 1u : 0u);
-      }
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss(tmem + dcol, desc_add(vdesc, (kk >> 2) * C::KV_BOX + (kk & 3) * 32),
+               desc_add(od, (kk >> 2) * C::Q_BOX + (kk & 3) * 32), ID_S, kk > 0 ? 1u : 0u);
     };
 
     bool ok = wait_warp(&bars->kv_full, 0, wc);
@@ -369,16 +366,16 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       if (!(ok = wait_warp(&bars->p_ready[it & 1], (it >> 1) & 1, wc))) break;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t ob = sdO + st * C::Q_TILE;
-        const uint32_t qb = sQ + st * C::Q_TILE;
+        const uint64_t od = desc_add(omn0, st * C::Q_TILE);
+        const uint64_t qd = desc_add(qmn0, st * C::Q_TILE);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)   // dV += P^T dO   (K = 64 queries)
-          mma_ts(tmem + C::DV_COL, tmem + C::SB_COL0 + 64 * buf + 8 * kk,
-                 smem_desc_sw128(ob + kk * 2048, C::Q_BOX, 1024), ID_KV, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::DV_COL, tmem + C::SB_COL0 + 64 * buf + 8 * kk, desc_add(od, kk * 2048), ID_KV,
+                 (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)   // dK += dS^T Q
-          mma_ts(tmem + C::DK_COL, tmem + C::PB_COL0 + 64 * buf + 8 * kk,
-                 smem_desc_sw128(qb + kk * 2048, C::Q_BOX, 1024), ID_KV, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::DK_COL, tmem + C::PB_COL0 + 64 * buf + 8 * kk, desc_add(qd, kk * 2048), ID_KV,
+                 (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars->q_empty[st]);
       }
       __syncwarp();
@@ -390,11 +387,11 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (it >= 1 && it + 1 >= n_iter && !(ok = wait_warp(&bars->dq_free, (it - 1) & 1, wc))) break;
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t dsb = sdS + buf * C::DS_BYTES;
+          const uint64_t dsd = desc_add(dsmn0, buf * C::DS_BYTES);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)   // dQ^T = K^T dS^T   (K = 128 keys)
-            mma_ss(tmem + C::PB_COL0 + 64 * buf, smem_desc_sw128(sK + kk * 2048, C::KV_BOX, 1024),
-                   smem_desc_sw128(dsb + kk * 2048, C::Q_BOX, 1024), ID_DQ, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + C::PB_COL0 + 64 * buf, desc_add(kmn, kk * 2048), desc_add(dsd, kk * 2048), ID_DQ,
+                   kk > 0 ? 1u : 0u);
           mma_commit(&bars->dq_full);
         }
         __syncwarp();
