@@ -176,23 +176,22 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const uint32_t sdO = smem_u32(smem + C::DO_OFF);
     const uint32_t sK = smem_u32(smem + C::K_OFF);
     const uint32_t sV = smem_u32(smem + C::V_OFF);
+    // Base descriptors, built once; each MMA's operand is an offset from them.
+    const uint64_t qdesc = smem_desc_sw128(sQ, 16, 1024), odesc = smem_desc_sw128(sdO, 16, 1024);
+    const uint64_t kdesc0 = smem_desc_sw128(sK, 16, 1024), vdesc0 = smem_desc_sw128(sV, 16, 1024);
+    const uint64_t kmn0 = smem_desc_sw128(sK, C::KV_BOX, 1024);
     auto issue_sdp = [&](int j) {
       const int st = j % C::STAGES;
       const uint32_t buf = (uint32_t)(j & 1);
+      const uint64_t kd = desc_add(kdesc0, st * C::KV_TILE), vd = desc_add(vdesc0, st * C::KV_TILE);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t offq = (kk >> 2) * C::Q_BOX + (kk & 3) * 32;
-        const uint32_t offk = (kk >> 2) * C::KV_BOX + (kk & 3) * 32;
-        mma_ss(tmem + C::S_COL + 64 * buf, smem_desc_sw128(sQ + offq, 16, 1024),
-               smem_desc_sw128(sK + st * C::KV_TILE + offk, 16, 1024), ID_S, kk > 0 ? 1u : 0u);
-      }
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss(tmem + C::S_COL + 64 * buf, desc_add(qdesc, (kk >> 2) * C::Q_BOX + (kk & 3) * 32),
+               desc_add(kd, (kk >> 2) * C::KV_BOX + (kk & 3) * 32), ID_S, kk > 0 ? 1u : 0u);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t offq = (kk >> 2) * C::Q_BOX + (kk & 3) * 32;
-        const uint32_t offk = (kk >> 2) * C::KV_BOX + (kk & 3) * 32;
-        mma_ss(tmem + C::DP_COL + 64 * buf, smem_desc_sw128(sdO + offq, 16, 1024),
-               smem_desc_sw128(sV + st * C::KV_TILE + offk, 16, 1024), ID_S, kk > 0 ? 1u : 0u);
-      }
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss(tmem + C::DP_COL + 64 * buf, desc_add(odesc, (kk >> 2) * C::Q_BOX + (kk & 3) * 32),
+               desc_add(vd, (kk >> 2) * C::KV_BOX + (kk & 3) * 32), ID_S, kk > 0 ? 1u : 0u);
       mma_commit(&bars->sdp_full[buf]);
     };
     bool ok = wait_warp(&bars->q_full, 0, wc);
@@ -211,8 +210,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)   // dQ += dS K   (K = 64 keys, 16 per MMA)
           mma_ts(tmem + C::DQ_COL, tmem + C::S_COL + 64 * buf + 8 * kk,
-                 smem_desc_sw128(sK + st * C::KV_TILE + kk * 2048, C::KV_BOX, 1024), ID_DQ,
-                 (j > 0 || kk > 0) ? 1u : 0u);
+                 desc_add(kmn0, st * C::KV_TILE + kk * 2048), ID_DQ, (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars->kv_empty[st]);
       }
       __syncwarp();

@@ -226,11 +226,15 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const uint32_t sK = smem_u32(smem + C::K_OFF);
     const uint32_t sV = smem_u32(smem + C::V_OFF);
     const uint32_t sP = smem_u32(smem + C::P_OFF);
+    // Base descriptors, built once; each MMA's operand is an offset from them.
+    const uint64_t qdesc = smem_desc_sw128(sQ, 16, 1024), pdesc = smem_desc_sw128(sP, 16, 1024);
+    const uint64_t kdesc0 = smem_desc_sw128(sK, 16, 1024), vdesc0 = smem_desc_sw128(sV, 16, 1024);
     const uint32_t colS[2] = {C::S_COL0, C::S_COL1};
     const uint32_t colO[2] = {C::O_COL0, C::O_COL1};
     bool ok = wait_warp(&bars->q_full, 0, wc);
     for (int j = 0; ok && j <= nkv_max; ++j) {
       const int sl = j % C::NS;                        // K_j and V_{j-1}
+      const uint64_t kdesc = desc_add(kdesc0, sl * C::TILE), vdesc = desc_add(vdesc0, sl * C::TILE);
       // TMA data needs no tcgen05 fence: the MMAs read it once the
       // transaction count of the slot's barrier has completed.
       if (!(ok = wait_warp(&bars->kv_full[sl], (j / C::NS) & 1, wc))) break;
@@ -242,8 +246,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           if (lane == 0) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)             // 32 keys per MMA
-              mma_ss_f8(tmem + colO[t], smem_desc_sw128(sP + t * C::TILE + kk * 32, 16, 1024),
-                        smem_desc_sw128(sV + sl * C::TILE + kk * 32, 16, 1024), IDESC,
+              mma_ss_f8(tmem + colO[t], desc_add(pdesc, t * C::TILE + kk * 32), desc_add(vdesc, kk * 32), IDESC,
                         (j - 1 > k0[t] || kk > 0) ? 1u : 0u);
           }
           __syncwarp();
@@ -252,8 +255,8 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           if (lane == 0) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)             // 32 head dims per MMA
-              mma_ss_f8(tmem + colS[t], smem_desc_sw128(sQ + t * C::TILE + kk * 32, 16, 1024),
-                        smem_desc_sw128(sK + sl * C::TILE + kk * 32, 16, 1024), IDESC, kk > 0 ? 1u : 0u);
+              mma_ss_f8(tmem + colS[t], desc_add(qdesc, t * C::TILE + kk * 32), desc_add(kdesc, kk * 32), IDESC,
+                        kk > 0 ? 1u : 0u);
             mma_commit(&bars->s_full[t]);
           }
           __syncwarp();
