@@ -140,7 +140,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, long long total_tokens) {
   if (B < 0 || Hq <= 0 || N < 0 || d <= 0 || total_tokens < 0) return 0;
   const long long T = total_tokens > 0 ? total_tokens : (long long)B * N;
-  return round256((size_t)Hq * T * sizeof(float)) + round256((size_t)Hq * T * d * sizeof(float));
+  return round256((size_t)Hq * T * sizeof(float)) + round256((size_t)Hq * T * d * sizeof(float)) + 256;
 }
 
 static fa_status bwd_impl(int stage, const void* q, const void* k, const void* v, const void* o,
@@ -181,6 +181,8 @@ static fa_status bwd_impl(int stage, const void* q, const void* k, const void* v
   p.D = static_cast<float*>(workspace);
   p.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                       round256((size_t)Hq * T * sizeof(float)));
+  p.work_ctr = reinterpret_cast<int*>(static_cast<char*>(workspace) + round256((size_t)Hq * T * sizeof(float)) +
+                                      round256((size_t)Hq * T * d * sizeof(float)));
   p.status = status_ptr();
   if (!p.status) return FA_ERR_CUDA;
   const int e = fa::launch_bwd_bf16(p, stream, stage);

@@ -10,11 +10,12 @@
 // Three kernels on the caller's stream:
 //   preprocess  D = rowsum(dO o O) in fp32 ([Hq, T]) and dQacc = 0
 //               ([Hq, T, d] fp32, head-major so a query tile is contiguous).
-//   dkdv        one CTA per (key tile of 128, kv head, sequence): loops over
-//               the query heads of the kv head's group and over query tiles
-//               of 64 (causal: only tiles at or after the key tile), keeping
-//               dK and dV in TMEM; each step's dQ contribution is added to
-//               dQacc with a bulk fp32 reduction from shared memory.
+//   dkdv        one persistent CTA per SM takes work items, each a (key tile
+//               of 128, kv head, sequence): it loops over the query heads of
+//               the kv head's group and over query tiles of 64 (causal: only
+//               tiles at or after the key tile), keeping dK and dV in TMEM;
+//               each step's dQ contribution is added to dQacc with a bulk
+//               fp32 reduction from shared memory.
 //   dq_convert  dQ = scale * dQacc -> bf16 [T, Hq, d].
 //
 // dkdv roles (320 threads):
@@ -37,6 +38,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "fa_host_util.h"
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
@@ -48,6 +51,7 @@ constexpr int kThreads = 320;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr int kQStages = 3;
+constexpr int kItemSlots = 4;     // ring of work-item indices passed to the roles
 
 template <int D>
 struct BwdCfg {
@@ -67,7 +71,7 @@ struct BwdCfg {
   static constexpr int DQ_OFF = DS_OFF + 2 * DS_BYTES;
   static constexpr int SIDE_OFF = DQ_OFF + DQ_BYTES;
   static constexpr int BAR_OFF = SIDE_OFF + kQStages * SIDE_BYTES;
-  static constexpr int SMEM_BYTES = BAR_OFF + 144 + 1024;
+  static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
   static constexpr uint32_t DV_COL = 0, DK_COL = D;
   static constexpr uint32_t SB_COL0 = 256, PB_COL0 = 384;   // + 64 * buffer
 };
@@ -78,10 +82,13 @@ struct BwdBars {
   uint64_t sdp_full[2];
   uint64_t p_ready[2];       // per step parity: arrivals can never run a phase ahead
   uint64_t dq_full, dq_free, dqs_free, dqs_full, dkdv_done;
+  uint64_t acc_free;                     // both epilogues have read dV and dK
+  uint64_t item_full[kItemSlots], item_empty[kItemSlots];
+  int item_q[kItemSlots];                // work item per slot, -1: no more
   uint32_t tmem_base;
   int abort_flag;
 };
-static_assert(sizeof(BwdBars) <= 144, "barrier block");
+static_assert(sizeof(BwdBars) <= 256, "barrier block");
 
 // Per-step query statistics, written by the producer warp:
 //   nL2[q] = -LSE_q * log2(e) - slope2 * q   (-inf for queries past the
@@ -100,7 +107,8 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 
 // ----------------------------------------------------------------- preprocess
 // D = dO . O in fp32 per (token, query head), and the dQ accumulator row
-// zeroed (not in the deterministic backward, which has no accumulator).
+// zeroed (not in the deterministic backward, which has no accumulator);
+// also the dK/dV kernel's work counters.
 // A thread takes 8 consecutive elements of a row (16-byte loads), D / 8
 // threads share a row, and each thread handles kPreRows rows, their loads
 // issued before any arithmetic so that enough bytes are in flight to stream
@@ -130,6 +138,9 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const AttnParams p)
   constexpr int G = D / 8;                       // threads per row
   constexpr int RPB = 256 / G;                   // rows per block and pass
   const int c8 = threadIdx.x % G;
+  // The dK/dV kernel's work-item counter and its count of finished CTAs
+  // start at zero (that kernel also puts them back to zero when it ends).
+  if (blockIdx.x == 0 && threadIdx.x < 2) p.work_ctr[threadIdx.x] = 0;
   const long long rows = p.T * p.Hq;
   float o_v[kPreRows][8], g_v[kPreRows][8];
   long long r[kPreRows];
@@ -185,6 +196,59 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const AttnParams p)
 }
 
 // ---------------------------------------------------------------------- dkdv
+// Work item w (a key tile of 128 rows of one kv head of one sequence) in
+// launch order.  Dense batches: key tile slowest, so with a causal mask the
+// first key tiles of every sequence and kv head (they meet the most query
+// tiles) are handed out first and the SMs are loaded longest-first.  Packed
+// batches hold many sequences of different lengths: there the key tiles of
+// one (sequence, kv head) are handed out together instead, so they share
+// its Q / dO stream through L2.
+struct DkdvItem {
+  int g, b, n0;          // kv head, sequence, first key row
+  long long seq0;        // first token of the sequence
+  int L;                 // sequence length
+  int qt0, nqt, n_iter;  // first query tile, query tiles per head, steps
+};
+
+template <bool CAUSAL, bool BAND>
+__device__ __forceinline__ bool dkdv_item(const AttnParams& p, int w, DkdvItem& it) {
+  const int nkt = (p.N + 127) / 128;
+  if (p.cu_seqlens) {
+    const int gb = w / nkt;
+    it.g = gb % p.Hkv;
+    it.b = gb / p.Hkv;
+    it.n0 = (w % nkt) * 128;
+  } else {
+    const int gb = w % (p.Hkv * p.B);
+    it.g = gb % p.Hkv;
+    it.b = gb / p.Hkv;
+    it.n0 = (w / (p.Hkv * p.B)) * 128;
+  }
+  if (!seq_bounds(p, it.b, &it.seq0, &it.L)) return false;
+  // Query tiles that see this key tile: all of them without a mask; under
+  // the causal mask those from the diagonal on, and with a sliding window w
+  // only those up to query n0 + 127 + w.
+  const int nqt_all = (it.L + 63) / 64;
+  it.qt0 = CAUSAL ? it.n0 / 64 : 0;
+  const int qt_end = BAND ? min(nqt_all, (it.n0 + 127 + p.window) / 64 + 1) : nqt_all;
+  it.nqt = qt_end - it.qt0;
+  it.n_iter = p.group * it.nqt;
+  return true;
+}
+
+// Persistent: one CTA per SM takes work items from a counter in the
+// workspace until none are left.  The producer
+// fetches an item and passes its index to the other roles through a ring of
+// four slots; every ring, barrier and buffer index continues across items
+// by a per-CTA step count, so the next item's Q/dO loads, its K/V load and
+// its first S/dP products overlap the previous item's last products and its
+// dK/dV epilogue.  Extra orderings at an item boundary:
+//   - K/V are single-buffered: the producer loads the next item's K/V once
+//     dkdv_done says every product of the previous item has completed;
+//   - the first dV/dK products of an item overwrite the accumulators, so
+//     they wait for acc_free: the compute warps have written the previous
+//     item's dV and dK out (both epilogues are theirs, so the dQ drain
+//     never waits for the end of an item and keeps pace with the products).
 // BAND: causal band (sliding window p.window); only with CAUSAL.
 // DQ: also accumulate dQ into the workspace (otherwise the deterministic
 // backward's dQ kernel computes it; this kernel then writes dK and dV only).
@@ -201,41 +265,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // 1-D grid.  Dense batches: key tile slowest, so with a causal mask the
-  // first key tiles of every sequence and kv head (they meet the most query
-  // tiles) are launched first and the SMs are loaded longest-first.  Packed
-  // batches hold many sequences of different lengths: there the key tiles
-  // of one (sequence, kv head) are launched together instead, so they share
-  // its Q / dO stream through L2.
-  const int nkt = (p.N + 127) / 128;
-  int g, b, n0;
-  if (p.cu_seqlens) {
-    const int gb = (int)(blockIdx.x / (unsigned)nkt);
-    g = gb % p.Hkv;
-    b = gb / p.Hkv;
-    n0 = (int)(blockIdx.x % (unsigned)nkt) * 128;
-  } else {
-    const int gb = (int)(blockIdx.x % (unsigned)(p.Hkv * p.B));
-    g = gb % p.Hkv;
-    b = gb / p.Hkv;
-    n0 = (int)(blockIdx.x / (unsigned)(p.Hkv * p.B)) * 128;
-  }
-  long long seq0;
-  int L;
-  if (!seq_bounds(p, b, &seq0, &L)) {
-    if (threadIdx.x == 0) record_status(p.status, FA_ERR_CU_SEQLENS);
-    return;
-  }
-  if (n0 >= L) return;
-  // Query tiles that see this key tile: all of them without a mask; under
-  // the causal mask those from the diagonal on, and with a sliding window w
-  // only those up to query n0 + 127 + w.
-  const int W = p.window;
-  const int nqt_all = (L + 63) / 64;
-  const int qt0 = CAUSAL ? n0 / 64 : 0;
-  const int qt_end = BAND ? min(nqt_all, (n0 + 127 + W) / 64 + 1) : nqt_all;
-  const int nqt = qt_end - qt0;             // query tiles per head (>= 1)
-  const int n_iter = p.group * nqt;
+  const int nwork = ((p.N + 127) / 128) * p.Hkv * p.B;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
@@ -252,6 +282,11 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     mbar_init(&bars->dqs_free, 1);
     mbar_init(&bars->dqs_full, 4);
     mbar_init(&bars->dkdv_done, 1);
+    mbar_init(&bars->acc_free, 4);                 // the 4 compute warps
+    for (int s = 0; s < kItemSlots; ++s) {
+      mbar_init(&bars->item_full[s], 1);
+      mbar_init(&bars->item_empty[s], 9);          // MMA warp + 4 compute + 4 drain warps
+    }
     bars->abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -265,6 +300,17 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const uint32_t tmem = bars->tmem_base;
   const WaitCtx wc{&bars->abort_flag, p.status};
 
+  // Consumers' view of the item ring: the k-th item's index, or -1 when the
+  // CTA is done (also on an abort).
+  auto next_item = [&](int k) -> int {
+    const int sl = k % kItemSlots;
+    if (!wait_warp(&bars->item_full[sl], (k / kItemSlots) & 1, wc)) return -1;
+    const int w = bars->item_q[sl];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->item_empty[sl]);
+    return w;
+  };
+
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -272,48 +318,93 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmdO);
-      mbar_arrive_expect_tx(&bars->kv_full, 2 * C::KV_TILE);
-#pragma unroll
-      for (int bx = 0; bx < C::NB; ++bx) {
-        tma_load_3d(smem + C::K_OFF + bx * C::KV_BOX, &tmK, bx * 64, g, (int)(seq0 + n0), &bars->kv_full);
-        tma_load_3d(smem + C::V_OFF + bx * C::KV_BOX, &tmV, bx * 64, g, (int)(seq0 + n0), &bars->kv_full);
-      }
     }
     __syncwarp();
-    int issued = 0;
-    for (int it = 0; it < n_iter; ++it) {
-      const int st = it % kQStages;
-      if (!wait_warp(&bars->q_empty[st], ((it / kQStages) & 1) ^ 1, wc)) break;
-      const int h = g * p.group + it / nqt;
-      const int q0 = (qt0 + it % nqt) * 64;
+    bool ok = true;
+    int G = 0;            // steps of the items before this one
+    int issued = 0;       // steps whose Q/dO loads were issued, over all items
+    int kv_loads = 0;     // K/V loads issued
+    for (int k = 0;; ++k) {
+      // Take the next item that has work (a key tile past a short packed
+      // sequence has none); a malformed cu_seqlens is recorded and skipped.
+      int w = 0;
+      DkdvItem it{};
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->q_full[st], 2 * C::Q_TILE);
-#pragma unroll
-        for (int bx = 0; bx < C::NB; ++bx) {
-          tma_load_3d(smem + C::Q_OFF + st * C::Q_TILE + bx * C::Q_BOX, &tmQ, bx * 64, h,
-                      (int)(seq0 + q0), &bars->q_full[st]);
-          tma_load_3d(smem + C::DO_OFF + st * C::Q_TILE + bx * C::Q_BOX, &tmdO, bx * 64, h,
-                      (int)(seq0 + q0), &bars->q_full[st]);
+        while (true) {
+          w = atomicAdd(p.work_ctr, 1);
+          if (w >= nwork) break;
+          if (!dkdv_item<CAUSAL, BAND>(p, w, it)) { record_status(p.status, FA_ERR_CU_SEQLENS); continue; }
+          if (it.n0 < it.L) break;
         }
       }
-      Side* sd = side + st;
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int qq = lane + 32 * r;
-        const bool valid = q0 + qq < L;
-        const long long idx = (long long)h * p.T + seq0 + q0 + qq;
-        const float sl2 = ALIBI ? __ldg(p.alibi + h) * kLog2e : 0.f;
-        sd->nL2[qq] = valid ? fmaf(-sl2, (float)qq, -__ldg(p.lse + idx) * kLog2e) : -INFINITY;
-        sd->Dv[qq] = valid ? __ldg(p.D + idx) : 0.f;
+      w = __shfl_sync(0xffffffffu, w, 0);
+      const int sl = k % kItemSlots;
+      if (!(ok = wait_warp(&bars->item_empty[sl], ((k / kItemSlots) & 1) ^ 1, wc))) break;
+      if (lane == 0) {
+        bars->item_q[sl] = w < nwork ? w : -1;
+        mbar_arrive(&bars->item_full[sl]);
       }
-      if (lane == 0) sd->slope2 = ALIBI ? __ldg(p.alibi + h) * kLog2e : 0.f;
       __syncwarp();
-      mbar_arrive(&bars->q_full[st]);
-      issued = it + 1;
+      if (w >= nwork) break;
+      dkdv_item<CAUSAL, BAND>(p, w, it);
+      auto load_step = [&](int i) -> bool {           // Q, dO and the side data of step G + i
+        const int s = G + i;
+        const int st = s % kQStages;
+        if (!wait_warp(&bars->q_empty[st], ((s / kQStages) & 1) ^ 1, wc)) return false;
+        const int h = it.g * p.group + i / it.nqt;
+        const int q0 = (it.qt0 + i % it.nqt) * 64;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars->q_full[st], 2 * C::Q_TILE);
+#pragma unroll
+          for (int bx = 0; bx < C::NB; ++bx) {
+            tma_load_3d(smem + C::Q_OFF + st * C::Q_TILE + bx * C::Q_BOX, &tmQ, bx * 64, h,
+                        (int)(it.seq0 + q0), &bars->q_full[st]);
+            tma_load_3d(smem + C::DO_OFF + st * C::Q_TILE + bx * C::Q_BOX, &tmdO, bx * 64, h,
+                        (int)(it.seq0 + q0), &bars->q_full[st]);
+          }
+        }
+        Side* sd = side + st;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int qq = lane + 32 * r;
+          const bool valid = q0 + qq < it.L;
+          const long long idx = (long long)h * p.T + it.seq0 + q0 + qq;
+          const float sl2 = ALIBI ? __ldg(p.alibi + h) * kLog2e : 0.f;
+          sd->nL2[qq] = valid ? fmaf(-sl2, (float)qq, -__ldg(p.lse + idx) * kLog2e) : -INFINITY;
+          sd->Dv[qq] = valid ? __ldg(p.D + idx) : 0.f;
+        }
+        if (lane == 0) sd->slope2 = ALIBI ? __ldg(p.alibi + h) * kLog2e : 0.f;
+        __syncwarp();
+        mbar_arrive(&bars->q_full[st]);
+        issued = s + 1;
+        return true;
+      };
+      // After the first item, the first two steps' Q/dO need only ring slots
+      // the previous item's last products free, while K/V must wait until
+      // all of them are done: those two go first.  On the first item K/V go
+      // first (the side data of a step waits for its loads of LSE and D).
+      const int pre = k > 0 ? min(2, it.n_iter) : 0;
+      for (int i = 0; ok && i < pre; ++i) ok = load_step(i);
+      if (!ok) break;
+      if (k > 0 && !(ok = wait_warp(&bars->dkdv_done, (k - 1) & 1, wc))) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->kv_full, 2 * C::KV_TILE);
+#pragma unroll
+        for (int bx = 0; bx < C::NB; ++bx) {
+          tma_load_3d(smem + C::K_OFF + bx * C::KV_BOX, &tmK, bx * 64, it.g, (int)(it.seq0 + it.n0), &bars->kv_full);
+          tma_load_3d(smem + C::V_OFF + bx * C::KV_BOX, &tmV, bx * 64, it.g, (int)(it.seq0 + it.n0), &bars->kv_full);
+        }
+      }
+      __syncwarp();
+      ++kv_loads;
+      for (int i = pre; ok && i < it.n_iter; ++i) ok = load_step(i);
+      if (!ok) break;
+      G += it.n_iter;
     }
-    wait_warp_drain(&bars->kv_full, 0);
-    for (int it = max(0, issued - kQStages); it < issued; ++it)
-      wait_warp_drain(&bars->q_full[it % kQStages], (it / kQStages) & 1);
+    // Loads in flight must land before this CTA's shared memory goes away.
+    if (kv_loads > 0) wait_warp_drain(&bars->kv_full, (kv_loads - 1) & 1);
+    for (int s = max(0, issued - kQStages); s < issued; ++s)
+      wait_warp_drain(&bars->q_full[s % kQStages], (s / kQStages) & 1);
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     constexpr uint32_t ID_S = idesc_bf16_f32(128, 64, 0, 0);   // S^T, dP^T
@@ -330,192 +421,259 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const uint64_t qmn0 = smem_desc_sw128(sQ, C::Q_BOX, 1024), omn0 = smem_desc_sw128(sdO, C::Q_BOX, 1024);
     const uint64_t kmn = smem_desc_sw128(sK, C::KV_BOX, 1024), dsmn0 = smem_desc_sw128(sdS, C::Q_BOX, 1024);
 
-    // S^T(i) into buffer i%2 and dP^T(i) into buffer i%2 (dP waits for the
-    // dQ drain of step i-2, which used the same columns).
-    auto issue_s = [&](int i) {
-      const uint64_t qd = desc_add(qdesc0, (i % kQStages) * C::Q_TILE);
-      const uint32_t dcol = C::SB_COL0 + 64 * (i & 1);
+    // Step s (counted over the CTA's items): S^T(s) and dP^T(s) into buffer
+    // s % 2, dQ^T(s) over dP^T(s).  dq_full is one barrier, so dq_full(s)
+    // may be committed only once the drain has taken dq_full(s - 1), i.e.
+    // once dq_free(s - 1) was waited; dP^T(s) overwrites dQ^T(s - 2), so it
+    // waits for dq_free(s - 2).  Inside an item both hold because dP(s + 2)
+    // waits for dq_free(s); need_dqf covers the first and last steps of an
+    // item.  dqf is the next dq_free phase to wait for.
+    int dqf = 0;
+    bool ok = true;
+    auto need_dqf = [&](int upto) -> bool {      // dq_free(0 .. upto) waited
+      if constexpr (!DQ) return true;
+      if (dqf > upto) return true;
+      do {
+        if (!wait_warp(&bars->dq_free, dqf & 1, wc)) return false;
+      } while (++dqf <= upto);
+      tc_fence_after();
+      return true;
+    };
+    auto issue_s = [&](int s) {
+      const uint64_t qd = desc_add(qdesc0, (s % kQStages) * C::Q_TILE);
+      const uint32_t dcol = C::SB_COL0 + 64 * (uint32_t)(s & 1);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         mma_ss(tmem + dcol, desc_add(kdesc, (kk >> 2) * C::KV_BOX + (kk & 3) * 32),
                desc_add(qd, (kk >> 2) * C::Q_BOX + (kk & 3) * 32), ID_S, kk > 0 ? 1u : 0u);
     };
-    auto issue_dp = [&](int i) {
-      const uint64_t od = desc_add(odesc0, (i % kQStages) * C::Q_TILE);
-      const uint32_t dcol = C::PB_COL0 + 64 * (i & 1);
+    auto issue_dp = [&](int s) {
+      const uint64_t od = desc_add(odesc0, (s % kQStages) * C::Q_TILE);
+      const uint32_t dcol = C::PB_COL0 + 64 * (uint32_t)(s & 1);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         mma_ss(tmem + dcol, desc_add(vdesc, (kk >> 2) * C::KV_BOX + (kk & 3) * 32),
                desc_add(od, (kk >> 2) * C::Q_BOX + (kk & 3) * 32), ID_S, kk > 0 ? 1u : 0u);
     };
 
-    bool ok = wait_warp(&bars->kv_full, 0, wc);
-    for (int i = 0; ok && i < 2 && i < n_iter; ++i) {
-      if (!(ok = wait_warp(&bars->q_full[i % kQStages], (i / kQStages) & 1, wc))) break;
-      tc_fence_after();
-      if (lane == 0) {
-        issue_s(i);
-        issue_dp(i);
-        mma_commit(&bars->sdp_full[i & 1]);
-      }
-      __syncwarp();
-    }
-    for (int it = 0; ok && it < n_iter; ++it) {
-      const int st = it % kQStages;
-      const int buf = it & 1;
-      if (!(ok = wait_warp(&bars->p_ready[it & 1], (it >> 1) & 1, wc))) break;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint64_t od = desc_add(omn0, st * C::Q_TILE);
-        const uint64_t qd = desc_add(qmn0, st * C::Q_TILE);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)   // dV += P^T dO   (K = 64 queries)
-          mma_ts(tmem + C::DV_COL, tmem + C::SB_COL0 + 64 * buf + 8 * kk, desc_add(od, kk * 2048), ID_KV,
-                 (it > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)   // dK += dS^T Q
-          mma_ts(tmem + C::DK_COL, tmem + C::PB_COL0 + 64 * buf + 8 * kk, desc_add(qd, kk * 2048), ID_KV,
-                 (it > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars->q_empty[st]);
-      }
-      __syncwarp();
-      if (DQ) {
-        // dq_full(it) must not complete before the drain has seen dq_full(it-1)
-        // (a skipped phase would leave the drain waiting for good).  Steps
-        // it-1 < n-2 already waited for that drain before dP(it+1); the last
-        // step did not, so it waits here.
-        if (it >= 1 && it + 1 >= n_iter && !(ok = wait_warp(&bars->dq_free, (it - 1) & 1, wc))) break;
-        tc_fence_after();
+    int G = 0;
+    int k = 0;
+    for (;; ++k) {
+      const int w = next_item(k);
+      if (w < 0) break;
+      DkdvItem it{};
+      dkdv_item<CAUSAL, BAND>(p, w, it);
+      const int G_end = G + it.n_iter;
+      if (!(ok = wait_warp(&bars->kv_full, k & 1, wc))) break;
+      // S/dP of the item's first two steps (Q/dO by TMA need no tcgen05
+      // fence once the stage's transaction count has completed)
+      for (int s = G; ok && s < G + 2 && s < G_end; ++s) {
+        if (!(ok = wait_warp(&bars->q_full[s % kQStages], (s / kQStages) & 1, wc))) break;
+        if (lane == 0) issue_s(s);
+        __syncwarp();
+        if (s >= 2 && !(ok = need_dqf(s - 2))) break;
         if (lane == 0) {
-          const uint64_t dsd = desc_add(dsmn0, buf * C::DS_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)   // dQ^T = K^T dS^T   (K = 128 keys)
-            mma_ss(tmem + C::PB_COL0 + 64 * buf, desc_add(kmn, kk * 2048), desc_add(dsd, kk * 2048), ID_DQ,
-                   kk > 0 ? 1u : 0u);
-          mma_commit(&bars->dq_full);
+          issue_dp(s);
+          mma_commit(&bars->sdp_full[s & 1]);
         }
         __syncwarp();
       }
-      const int nx = it + 2;
-      if (nx < n_iter) {
-        if (!(ok = wait_warp(&bars->q_full[nx % kQStages], (nx / kQStages) & 1, wc))) break;
+      if (!ok) break;
+      // The item's first dV/dK products overwrite the accumulators the
+      // previous item's epilogues read.
+      if (k > 0) {
+        if (!(ok = wait_warp(&bars->acc_free, (k - 1) & 1, wc))) break;
         tc_fence_after();
-        if (lane == 0) issue_s(nx);
-        __syncwarp();
-        // dP(nx) reuses the columns of dQ^T(it) (DQ) or of dS^T(it), which
-        // the dK(it) MMA issued above reads first (MMAs run in issue order)
-        if (DQ && !(ok = wait_warp(&bars->dq_free, it & 1, wc))) break;
+      }
+      for (int s = G; s < G_end; ++s) {
+        const int st = s % kQStages;
+        const uint32_t buf = (uint32_t)(s & 1);
+        if (!(ok = wait_warp(&bars->p_ready[buf], (s >> 1) & 1, wc))) break;
         tc_fence_after();
         if (lane == 0) {
-          issue_dp(nx);
-          mma_commit(&bars->sdp_full[buf]);
+          const uint64_t od = desc_add(omn0, st * C::Q_TILE);
+          const uint64_t qd = desc_add(qmn0, st * C::Q_TILE);
+          const uint32_t acc0 = s > G ? 1u : 0u;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)   // dV += P^T dO   (K = 64 queries)
+            mma_ts(tmem + C::DV_COL, tmem + C::SB_COL0 + 64 * buf + 8 * kk, desc_add(od, kk * 2048), ID_KV,
+                   kk > 0 ? 1u : acc0);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)   // dK += dS^T Q
+            mma_ts(tmem + C::DK_COL, tmem + C::PB_COL0 + 64 * buf + 8 * kk, desc_add(qd, kk * 2048), ID_KV,
+                   kk > 0 ? 1u : acc0);
+          mma_commit(&bars->q_empty[st]);
         }
         __syncwarp();
+        if (DQ) {
+          // the item's first and last steps: dq_free(s - 1) may be pending
+          if ((s == G || s + 1 == G_end) && s >= 1 && !(ok = need_dqf(s - 1))) break;
+          if (lane == 0) {
+            const uint64_t dsd = desc_add(dsmn0, buf * C::DS_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)   // dQ^T = K^T dS^T   (K = 128 keys)
+              mma_ss(tmem + C::PB_COL0 + 64 * buf, desc_add(kmn, kk * 2048), desc_add(dsd, kk * 2048), ID_DQ,
+                     kk > 0 ? 1u : 0u);
+            mma_commit(&bars->dq_full);
+          }
+          __syncwarp();
+        }
+        // S/dP two steps ahead, within the item (the next item's first two
+        // need its K/V, loaded once this item's products are done).
+        const int nx = s + 2;
+        if (nx < G_end) {
+          if (!(ok = wait_warp(&bars->q_full[nx % kQStages], (nx / kQStages) & 1, wc))) break;
+          if (lane == 0) issue_s(nx);
+          __syncwarp();
+          // dP(nx) reuses the columns of dQ^T(s) (DQ) or of dS^T(s), which
+          // the dK(s) MMA issued above reads first (MMAs run in issue order)
+          if (DQ) {
+            if (!(ok = wait_warp(&bars->dq_free, s & 1, wc))) break;
+            dqf = s + 1;
+            tc_fence_after();
+          }
+          if (lane == 0) {
+            issue_dp(nx);
+            mma_commit(&bars->sdp_full[buf]);
+          }
+          __syncwarp();
+        }
       }
+      if (!ok) break;
+      if (lane == 0) mma_commit(&bars->dkdv_done);
+      __syncwarp();
+      G = G_end;
     }
-    if (lane == 0) mma_commit(&bars->dkdv_done);
-    __syncwarp();
-    wait_warp_drain(&bars->dkdv_done, 0);
+    // Tensor-core work must be finished before the TMEM is released; after
+    // an abort in the middle of an item, one more commit covers what it
+    // issued.
+    int commits = k;
+    if (!ok) {
+      if (lane == 0) mma_commit(&bars->dkdv_done);
+      __syncwarp();
+      ++commits;
+    }
+    if (commits > 0) wait_warp_drain(&bars->dkdv_done, (commits - 1) & 1);
   } else if (warp < 4) {
     // ------------------------------------------------------------- compute
     const int kr = 32 * warp + lane;          // key row within the tile
-    const int key = n0 + kr;
-    const bool key_ok = key < L;
     const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
     const float c2 = p.scale_log2;
     bool ok = true;
-    for (int it = 0; it < n_iter; ++it) {
-      const int st = it % kQStages;
-      const int buf = it & 1;
-      const int q0 = (qt0 + it % nqt) * 64;
-      if (!(ok = wait_warp(&bars->sdp_full[buf], (it >> 1) & 1, wc))) break;
-      tc_fence_after();
-      const Side* sd = side + st;
-      const bool need_mask = (CAUSAL && q0 < n0 + 127) || (BAND && q0 + 63 > n0 + W) || !key_ok;
-      // x = S^T * scale * log2(e) + slope2 * (key - q0) + nL2[q]: the bias
-      // term is split into a per-thread part (key - q0, exact integer) and a
-      // per-query part folded into nL2 by the producer.
-      const float kb = ALIBI ? sd->slope2 * (float)(key - q0) : 0.f;
-      const uint64_t c2p = f2(c2, c2);
-      const uint64_t kbp = f2(kb, kb);
-      uint8_t* dsrow = smem + C::DS_OFF + buf * C::DS_BYTES + kr * 128;
-      const uint32_t tSb = lane_base + C::SB_COL0 + 64 * buf;
-      const uint32_t tPb = lane_base + C::PB_COL0 + 64 * buf;
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {    // 32 queries at a time
-        uint32_t sv[32], dp[32];
-        tmem_ld32(tSb + 32 * half, sv);
-        tmem_ld32(tPb + 32 * half, dp);
-        tmem_wait_ld();
-        reg_fence32(sv);
-        reg_fence32(dp);
-        uint32_t pk[16], dk[16];
-        const float4* nl4 = reinterpret_cast<const float4*>(sd->nL2 + 32 * half);
-        const float4* dd4 = reinterpret_cast<const float4*>(sd->Dv + 32 * half);
-#pragma unroll
-        for (int g4 = 0; g4 < 8; ++g4) {        // 4 queries per group
-          const float4 nl = nl4[g4];
-          const float4 dd = dd4[g4];
-#pragma unroll
-          for (int pr = 0; pr < 2; ++pr) {
-            const int ql = 4 * g4 + 2 * pr;     // query within the half
-            uint64_t bias = pr ? f2(nl.z, nl.w) : f2(nl.x, nl.y);
-            if (ALIBI) bias = fadd2(bias, kbp);
-            float x0, x1;
-            f2split(ffma2(f2(__uint_as_float(sv[ql]), __uint_as_float(sv[ql + 1])), c2p, bias), x0, x1);
-            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            if (need_mask) {
-              const int q = q0 + 32 * half + ql;
-              if (!key_ok || (CAUSAL && key > q) || (BAND && q > key + W)) p0 = 0.f;
-              if (!key_ok || (CAUSAL && key > q + 1) || (BAND && q + 1 > key + W)) p1 = 0.f;
+    int G = 0;
+    for (int k = 0; ok; ++k) {
+      const int w = next_item(k);
+      if (w < 0) break;
+      DkdvItem itm{};
+      dkdv_item<CAUSAL, BAND>(p, w, itm);
+      const int n0 = itm.n0, L = itm.L, nqt = itm.nqt;
+      const int key = n0 + kr;
+      const bool key_ok = key < L;
+      for (int i = 0; i < itm.n_iter; ++i) {
+        const int s = G + i;
+        const int st = s % kQStages;
+        const int buf = s & 1;
+        const int q0 = (itm.qt0 + i % nqt) * 64;
+        if (!(ok = wait_warp(&bars->sdp_full[buf], (s >> 1) & 1, wc))) break;
+        tc_fence_after();
+        const Side* sd = side + st;
+        const bool need_mask = (CAUSAL && q0 < n0 + 127) || (BAND && q0 + 63 > n0 + p.window) || !key_ok;
+        // x = S^T * scale * log2(e) + slope2 * (key - q0) + nL2[q]: the bias
+        // term is split into a per-thread part (key - q0, exact integer) and a
+        // per-query part folded into nL2 by the producer.
+        const float kb = ALIBI ? sd->slope2 * (float)(key - q0) : 0.f;
+        const uint64_t c2p = f2(c2, c2);
+        const uint64_t kbp = f2(kb, kb);
+        uint8_t* dsrow = smem + C::DS_OFF + buf * C::DS_BYTES + kr * 128;
+        const uint32_t tSb = lane_base + C::SB_COL0 + 64 * buf;
+        const uint32_t tPb = lane_base + C::PB_COL0 + 64 * buf;
+  #pragma unroll 1
+        for (int half = 0; half < 2; ++half) {    // 32 queries at a time
+          uint32_t sv[32], dp[32];
+          tmem_ld32(tSb + 32 * half, sv);
+          tmem_ld32(tPb + 32 * half, dp);
+          tmem_wait_ld();
+          reg_fence32(sv);
+          reg_fence32(dp);
+          uint32_t pk[16], dk[16];
+          const float4* nl4 = reinterpret_cast<const float4*>(sd->nL2 + 32 * half);
+          const float4* dd4 = reinterpret_cast<const float4*>(sd->Dv + 32 * half);
+  #pragma unroll
+          for (int g4 = 0; g4 < 8; ++g4) {        // 4 queries per group
+            const float4 nl = nl4[g4];
+            const float4 dd = dd4[g4];
+  #pragma unroll
+            for (int pr = 0; pr < 2; ++pr) {
+              const int ql = 4 * g4 + 2 * pr;     // query within the half
+              uint64_t bias = pr ? f2(nl.z, nl.w) : f2(nl.x, nl.y);
+              if (ALIBI) bias = fadd2(bias, kbp);
+              float x0, x1;
+              f2split(ffma2(f2(__uint_as_float(sv[ql]), __uint_as_float(sv[ql + 1])), c2p, bias), x0, x1);
+              float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              if (need_mask) {
+                const int q = q0 + 32 * half + ql;
+                if (!key_ok || (CAUSAL && key > q) || (BAND && q > key + p.window)) p0 = 0.f;
+                if (!key_ok || (CAUSAL && key > q + 1) || (BAND && q + 1 > key + p.window)) p1 = 0.f;
+              }
+              const uint64_t pp = f2(p0, p1);
+              const uint64_t dsd = fmul2(pp, fsub2(f2(__uint_as_float(dp[ql]), __uint_as_float(dp[ql + 1])),
+                                                   pr ? f2(dd.z, dd.w) : f2(dd.x, dd.y)));
+              float d0, d1;
+              f2split(dsd, d0, d1);
+              pk[ql / 2] = pack_bf16x2(p0, p1);
+              dk[ql / 2] = pack_bf16x2(d0, d1);
             }
-            const uint64_t pp = f2(p0, p1);
-            const uint64_t dsd = fmul2(pp, fsub2(f2(__uint_as_float(dp[ql]), __uint_as_float(dp[ql + 1])),
-                                                 pr ? f2(dd.z, dd.w) : f2(dd.x, dd.y)));
-            float d0, d1;
-            f2split(dsd, d0, d1);
-            pk[ql / 2] = pack_bf16x2(p0, p1);
-            dk[ql / 2] = pack_bf16x2(d0, d1);
+          }
+          tmem_st16(tSb + 16 * half, pk);          // P^T (bf16) over consumed S^T columns
+          tmem_st16(tPb + 16 * half, dk);          // dS^T (bf16) over consumed dP^T columns
+          if (DQ) {
+  #pragma unroll
+            for (int q16 = 0; q16 < 4; ++q16) {    // dS^T row into shared memory (swizzled)
+              const int chunk = 4 * half + q16;
+              const int phys = chunk ^ (kr & 7);
+              *reinterpret_cast<uint4*>(dsrow + phys * 16) =
+                  make_uint4(dk[4 * q16], dk[4 * q16 + 1], dk[4 * q16 + 2], dk[4 * q16 + 3]);
+            }
           }
         }
-        tmem_st16(tSb + 16 * half, pk);          // P^T (bf16) over consumed S^T columns
-        tmem_st16(tPb + 16 * half, dk);          // dS^T (bf16) over consumed dP^T columns
-        if (DQ) {
+        if (DQ) fence_proxy_async_smem();
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_ready[buf]);
+      }
+      if (!ok) break;
+      // dV and dK epilogues (one key row per thread), then the accumulators
+      // are free for the next item
+      if (!(ok = wait_warp(&bars->dkdv_done, k & 1, wc))) break;
+      tc_fence_after();
+      const float sc = p.scale;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {        // 0: dV, 1: dK (times the scale)
+        const float f = which ? sc : 1.f;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(which ? p.dk : p.dv) +
+                             ((itm.seq0 + key) * p.Hkv + itm.g) * D;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(lane_base + (which ? C::DK_COL : C::DV_COL) + c0, r);
+          tmem_wait_ld();
+          reg_fence32(r);
+          uint32_t pkd[16];
 #pragma unroll
-          for (int q16 = 0; q16 < 4; ++q16) {    // dS^T row into shared memory (swizzled)
-            const int chunk = 4 * half + q16;
-            const int phys = chunk ^ (kr & 7);
-            *reinterpret_cast<uint4*>(dsrow + phys * 16) =
-                make_uint4(dk[4 * q16], dk[4 * q16 + 1], dk[4 * q16 + 2], dk[4 * q16 + 3]);
+          for (int e = 0; e < 16; ++e)
+            pkd[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * f, __uint_as_float(r[2 * e + 1]) * f);
+          if (key_ok) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) d4[v4] = make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
           }
         }
       }
-      if (DQ) fence_proxy_async_smem();
-      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_ready[it & 1]);
-    }
-    // dV epilogue
-    if (ok) ok = wait_warp(&bars->dkdv_done, 0, wc);
-    if (ok) {
-      tc_fence_after();
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.dv) + ((seq0 + key) * p.Hkv + g) * D;
-#pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(lane_base + C::DV_COL + c0, r);
-        tmem_wait_ld();
-        reg_fence32(r);
-        uint32_t pkd[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) pkd[c] = pack_bf16x2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]));
-        if (key_ok) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) d4[v4] = make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
-        }
-      }
+      if (lane == 0) mbar_arrive(&bars->acc_free);
+      G += itm.n_iter;
     }
   } else {
     // ------------------------------------------------------------ dQ drain
@@ -524,69 +682,55 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const uint32_t lane_base = tmem + ((uint32_t)(32 * q4) << 16);
     float* dqs = reinterpret_cast<float*>(smem + C::DQ_OFF);
     bool ok = true;
-    for (int it = 0; DQ && it < n_iter; ++it) {
-      const int buf = it & 1;
-      const int h = g * p.group + it / nqt;
-      const int q0 = (qt0 + it % nqt) * 64;
-      const int nvalid = min(64, L - q0);
-      if (!(ok = wait_warp(&bars->dq_full, it & 1, wc))) break;
-      tc_fence_after();
-      uint32_t r[64];
-      tmem_ld32(lane_base + C::PB_COL0 + 64 * buf, r);
-      tmem_ld32(lane_base + C::PB_COL0 + 64 * buf + 32, r + 32);
-      tmem_wait_ld();
-      reg_fence32(r);
-      reg_fence32(r + 32);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->dq_free);
-      if (!(ok = wait_warp(&bars->dqs_free, (it & 1) ^ 1, wc))) break;
-      if (c < D) {
-#pragma unroll
-        for (int qq = 0; qq < 64; ++qq) dqs[qq * D + c] = __uint_as_float(r[qq]);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->dqs_full);
-      if (q4 == 0) {
-        if (!(ok = wait_warp(&bars->dqs_full, it & 1, wc))) break;
-        if (lane == 0) {
-          bulk_reduce_add_f32(p.dq_acc + ((long long)h * p.T + seq0 + q0) * D, dqs,
-                              (uint32_t)(nvalid * D * 4));
-          bulk_commit_group();
-          bulk_wait_group_read0();
-          mbar_arrive(&bars->dqs_free);
-        }
+    int G = 0;
+    for (int k = 0; ok; ++k) {
+      const int w = next_item(k);
+      if (w < 0) break;
+      DkdvItem itm{};
+      dkdv_item<CAUSAL, BAND>(p, w, itm);
+      for (int i = 0; DQ && i < itm.n_iter; ++i) {
+        const int s = G + i;
+        const int buf = s & 1;
+        const int h = itm.g * p.group + i / itm.nqt;
+        const int q0 = (itm.qt0 + i % itm.nqt) * 64;
+        const int nvalid = min(64, itm.L - q0);
+        if (!(ok = wait_warp(&bars->dq_full, s & 1, wc))) break;
+        tc_fence_after();
+        uint32_t r[64];
+        tmem_ld32(lane_base + C::PB_COL0 + 64 * buf, r);
+        tmem_ld32(lane_base + C::PB_COL0 + 64 * buf + 32, r + 32);
+        tmem_wait_ld();
+        reg_fence32(r);
+        reg_fence32(r + 32);
+        tc_fence_before();
         __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->dq_free);
+        if (!(ok = wait_warp(&bars->dqs_free, (s & 1) ^ 1, wc))) break;
+        if (c < D) {
+#pragma unroll
+          for (int qq = 0; qq < 64; ++qq) dqs[qq * D + c] = __uint_as_float(r[qq]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->dqs_full);
+        if (q4 == 0) {
+          if (!(ok = wait_warp(&bars->dqs_full, s & 1, wc))) break;
+          if (lane == 0) {
+            bulk_reduce_add_f32(p.dq_acc + ((long long)h * p.T + itm.seq0 + q0) * D, dqs,
+                                (uint32_t)(nvalid * D * 4));
+            bulk_commit_group();
+            bulk_wait_group_read0();
+            mbar_arrive(&bars->dqs_free);
+          }
+          __syncwarp();
+        }
       }
+      if (!ok) break;
+      G += itm.n_iter;
     }
+    // The dQ reductions still in flight must finish before the kernel ends.
     if (DQ && q4 == 0 && lane == 0) bulk_wait_group0();
     __syncwarp();
-    // dK epilogue
-    if (ok) ok = wait_warp(&bars->dkdv_done, 0, wc);
-    if (ok) {
-      tc_fence_after();
-      const int key = n0 + c;
-      const bool key_ok = key < L;
-      const float sc = p.scale;
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.dk) + ((seq0 + key) * p.Hkv + g) * D;
-#pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t rr[32];
-        tmem_ld32(lane_base + C::DK_COL + c0, rr);
-        tmem_wait_ld();
-        reg_fence32(rr);
-        uint32_t pkd[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pkd[e] = pack_bf16x2(__uint_as_float(rr[2 * e]) * sc, __uint_as_float(rr[2 * e + 1]) * sc);
-        if (key_ok) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) d4[v4] = make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
-        }
-      }
-    }
   }
 
   tc_fence_before();
@@ -594,6 +738,16 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
+  }
+  // The last CTA to finish (all have stopped taking items by then) puts the
+  // counters back to zero, so the next launch on this workspace starts
+  // from item 0 even without the preprocess.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.work_ctr + 1, 1) == (int)gridDim.x - 1) {
+      p.work_ctr[0] = 0;
+      p.work_ctr[1] = 0;
+    }
   }
 }
 
@@ -609,7 +763,15 @@ int launch_dkdv(const AttnParams& p, cudaStream_t stream) {
   if (!r) r = make_tmap_bf16_3d(&tk, p.k, D, p.Hkv, p.T, 128);
   if (!r) r = make_tmap_bf16_3d(&tv, p.v, D, p.Hkv, p.T, 128);
   if (r) return r;
-  dim3 grid((unsigned)(((p.N + 127) / 128) * p.Hkv * p.B));
+  // Persistent: one CTA per SM (at most one per item), items handed out by
+  // the workspace counter (zeroed by the preprocess and by the previous
+  // launch's last CTA).
+  const long long nwork = (long long)((p.N + 127) / 128) * p.Hkv * p.B;
+  int dev = 0, nsm = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return (int)e;
+  dim3 grid((unsigned)std::min<long long>(nwork, nsm));
   kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, p);
   return (int)cudaGetLastError();
 }

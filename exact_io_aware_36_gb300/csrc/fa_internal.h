@@ -31,6 +31,7 @@ struct AttnParams {
   void* dv;
   float* D;          // workspace: D_i = dO_i . O_i, [Hq, T]
   float* dq_acc;     // workspace: fp32 dQ accumulator, [Hq, T, d]
+  int* work_ctr;     // workspace: dK/dV work-item counter, finished-CTA count
   const int32_t* cu_seqlens;   // [B+1] or nullptr
   const float* alibi;          // [Hq] or nullptr
   unsigned int* status;        // per-device status word

@@ -104,11 +104,11 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  void* stream);
 
 /*
- * Bytes of device workspace fa_bwd needs: D (float32 [Hq, T]) and the dQ
- * accumulator (float32 [Hq, T, d]), each 256-byte aligned.  T is
- * total_tokens when > 0, else B*N.  Returns 0 for invalid sizes.  The
- * deterministic backward uses only the first part (D); this size serves
- * both.
+ * Bytes of device workspace fa_bwd needs: D (float32 [Hq, T]), the dQ
+ * accumulator (float32 [Hq, T, d]) and 256 bytes for the dK/dV kernel's
+ * work-item counter, each part 256-byte aligned.  T is total_tokens when
+ * > 0, else B*N.  Returns 0 for invalid sizes.  The deterministic backward
+ * does not use the accumulator; this size serves both.
  */
 size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, long long total_tokens);
 
