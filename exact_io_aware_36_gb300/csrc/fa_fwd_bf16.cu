@@ -57,6 +57,8 @@ struct FwdCfg {
   static constexpr int V_OFF = K_OFF + NS * TILE_BYTES;
   static constexpr int BAR_OFF = V_OFF + NS * TILE_BYTES;
   static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
+  // The epilogue stages both tiles' O (fp32 at most) in the K/V slots.
+  static_assert(2 * 128 * D * 4 <= BAR_OFF - K_OFF, "O staging must fit the K/V slots");
   static constexpr uint32_t S_COL0 = 0, S_COL1 = 128;
   static constexpr uint32_t O_COL0 = 256, O_COL1 = 256 + D;
 };
@@ -78,7 +80,8 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 template <int D, bool CAUSAL, bool ALIBI, bool BAND>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                const AttnParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -413,43 +416,81 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       if (lane == 0) mbar_arrive(&bars->p_full[t]);
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && nkv[t] > 0) ok = wait_warp(&bars->o_done, 0, wc);
-    if (ok && nkv[t] > 0) {
-      tc_fence_after();
+    // O = acc / l~ per row and LSE.  A tile whose 128 rows all lie in the
+    // sequence is staged in shared memory (the K/V slots, free once every
+    // product is done) in the TMA box layout (128-byte rows, 16-byte chunks
+    // swizzled by row) and written by TMA stores: whole rows at a time
+    // instead of 32 scattered 16-byte pieces per warp instruction.  A tile
+    // that crosses the sequence end keeps per-thread stores of its valid
+    // rows (a box would overwrite the next sequence's rows).
+    if (nkv[t] > 0) {                          // uniform over the tile's warps
+      if (ok) ok = wait_warp(&bars->o_done, 0, wc);
+      const bool full_tile = m0 + 128 * t + 128 <= L;
+      const int r = 32 * q4 + lane;            // row within the tile
+      const int esz = p.o_f32 ? 4 : 2;
+      uint8_t* stg = smem + C::K_OFF + t * (128 * D * 4);
       const bool valid = row < L;
       const float inv = lr > 0.f ? 1.f / lr : 0.f;
       const long long tok = seq0 + row;
+      if (ok) {
+        tc_fence_after();
 #pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t o[32];
-        tmem_ld32(tO + c0, o);
-        tmem_wait_ld();
-        reg_fence32(o);
-        if (p.o_f32) {
-          float* O = static_cast<float*>(p.o) + (tok * p.Hq + h) * D + c0;
-          if (valid) {
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + c0, o);
+          tmem_wait_ld();
+          reg_fence32(o);
+          if (p.o_f32) {
+            float4 v[8];
 #pragma unroll
             for (int v4 = 0; v4 < 8; ++v4)
-              reinterpret_cast<float4*>(O)[v4] =
-                  make_float4(__uint_as_float(o[4 * v4]) * inv, __uint_as_float(o[4 * v4 + 1]) * inv,
-                              __uint_as_float(o[4 * v4 + 2]) * inv, __uint_as_float(o[4 * v4 + 3]) * inv);
-          }
-        } else {
-          __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o) + (tok * p.Hq + h) * D + c0;
-          uint32_t pkd[16];
+              v[v4] = make_float4(__uint_as_float(o[4 * v4]) * inv, __uint_as_float(o[4 * v4 + 1]) * inv,
+                                  __uint_as_float(o[4 * v4 + 2]) * inv, __uint_as_float(o[4 * v4 + 3]) * inv);
+            if (full_tile) {                   // box c0 / 32: this row's 128 bytes
+              uint8_t* rowp = stg + (c0 / 32) * 16384 + r * 128;
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
-            pkd[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
-          if (valid) {
+              for (int cc = 0; cc < 8; ++cc) *reinterpret_cast<float4*>(rowp + ((cc ^ (r & 7)) << 4)) = v[cc];
+            } else if (valid) {
+              float* O = static_cast<float*>(p.o) + (tok * p.Hq + h) * D + c0;
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              reinterpret_cast<uint4*>(O)[v4] =
-                  make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
+              for (int v4 = 0; v4 < 8; ++v4) reinterpret_cast<float4*>(O)[v4] = v[v4];
+            }
+          } else {
+            uint32_t pkd[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+              pkd[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
+            if (full_tile) {                   // box c0 / 64: chunks (c0 % 64) / 8 .. + 3 of this row
+              uint8_t* rowp = stg + (c0 / 64) * 16384 + r * 128;
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc)
+                *reinterpret_cast<uint4*>(rowp + ((((c0 % 64) / 8 + cc) ^ (r & 7)) << 4)) =
+                    make_uint4(pkd[4 * cc], pkd[4 * cc + 1], pkd[4 * cc + 2], pkd[4 * cc + 3]);
+            } else if (valid) {
+              __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o) + (tok * p.Hq + h) * D + c0;
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4)
+                reinterpret_cast<uint4*>(O)[v4] =
+                    make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
+            }
           }
         }
+        if (valid)
+          p.lse[(long long)h * p.T + tok] = l > 0.f ? (m_ref + lg2_approx(l)) * kLn2 : -INFINITY;
       }
-      if (valid)
-        p.lse[(long long)h * p.T + tok] = l > 0.f ? (m_ref + lg2_approx(l)) * kLn2 : -INFINITY;
+      if (full_tile) {
+        // Every warp of the tile reaches this barrier (also after an abort);
+        // the stores go out only if all four staged their rows.
+        fence_proxy_async_smem();
+        const bool any_bad = named_bar_any(1 + t, 128, !ok);
+        if (!any_bad && q4 == 0 && lane == 0) {
+          const int boxes = (D * esz) / 128;
+          for (int bx = 0; bx < boxes; ++bx)
+            tma_store_3d(&tmO, stg + bx * 16384, bx * (128 / esz), h, (int)(seq0 + m0 + 128 * t));
+          bulk_commit_group();
+          bulk_wait_group0();                  // shared memory must outlive the stores
+        }
+      }
     }
   }
 
@@ -468,13 +509,14 @@ int launch_impl(const AttnParams& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return (int)e;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   int r = make_tmap_bf16_3d(&tq, p.q, D, p.Hq, p.T, 128);
   if (!r) r = make_tmap_bf16_3d(&tk, p.k, D, p.Hkv, p.T, 128);
   if (!r) r = make_tmap_bf16_3d(&tv, p.v, D, p.Hkv, p.T, 128);
+  if (!r) r = p.o_f32 ? make_tmap_f32_3d(&to, p.o, D, p.Hq, p.T, 128) : make_tmap_bf16_3d(&to, p.o, D, p.Hq, p.T, 128);
   if (r) return r;
   dim3 grid((unsigned)(((p.N + 255) / 256) * p.Hq * p.B));
-  kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, to, p);
   return (int)cudaGetLastError();
 }
 

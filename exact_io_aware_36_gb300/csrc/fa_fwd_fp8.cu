@@ -52,6 +52,8 @@ struct Cfg {
   static constexpr int P_OFF = V_OFF + NS * TILE;
   static constexpr int BAR_OFF = P_OFF + 2 * TILE;
   static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
+  // The epilogue stages both tiles' O (fp32 at most) in the K/V slots.
+  static_assert(2 * 128 * kD * 4 <= P_OFF - K_OFF, "O staging must fit the K/V slots");
   static constexpr uint32_t S_COL0 = 0, S_COL1 = 128;
   static constexpr uint32_t O_COL0 = 256, O_COL1 = 384;
 };
@@ -116,7 +118,8 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 template <bool CAUSAL, bool ALIBI, bool BAND>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-               const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+               const AttnParams p) {
   using C = Cfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -428,42 +431,77 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       if (lane == 0) mbar_arrive(&bars->p_full[t]);
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && nkv[t] > 0) ok = wait_warp(&bars->o_done, 0, wc);
-    if (ok && nkv[t] > 0) {
-      tc_fence_after();
+    // O and LSE as in the bf16 forward: a tile whose 128 rows all lie in the
+    // sequence is staged in the K/V slots in the TMA box layout and written
+    // by TMA stores; a tile crossing the sequence end keeps per-thread
+    // stores of its valid rows.
+    if (nkv[t] > 0) {                          // uniform over the tile's warps
+      if (ok) ok = wait_warp(&bars->o_done, 0, wc);
+      const bool full_tile = m0 + 128 * t + 128 <= L;
+      const int r = 32 * q4 + lane;            // row within the tile
+      const int esz = p.o_f32 ? 4 : 2;
+      uint8_t* stg = smem + C::K_OFF + t * (128 * kD * 4);
       const bool valid = row < L;
       const float inv = lr > 0.f ? vmax / lr : 0.f;
       const long long tok = seq0 + row;
+      if (ok) {
+        tc_fence_after();
 #pragma unroll 1
-      for (int cb = 0; cb < kD; cb += 32) {
-        uint32_t o[32];
-        tmem_ld32(tO + cb, o);
-        tmem_wait_ld();
-        reg_fence32(o);
-        if (p.o_f32) {
-          float* O = static_cast<float*>(p.o) + (tok * p.Hq + h) * kD + cb;
-          if (valid) {
+        for (int cb = 0; cb < kD; cb += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + cb, o);
+          tmem_wait_ld();
+          reg_fence32(o);
+          if (p.o_f32) {
+            float4 v[8];
 #pragma unroll
             for (int v4 = 0; v4 < 8; ++v4)
-              reinterpret_cast<float4*>(O)[v4] =
-                  make_float4(__uint_as_float(o[4 * v4]) * inv, __uint_as_float(o[4 * v4 + 1]) * inv,
-                              __uint_as_float(o[4 * v4 + 2]) * inv, __uint_as_float(o[4 * v4 + 3]) * inv);
-          }
-        } else {
-          __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o) + (tok * p.Hq + h) * kD + cb;
-          uint32_t pkd[16];
+              v[v4] = make_float4(__uint_as_float(o[4 * v4]) * inv, __uint_as_float(o[4 * v4 + 1]) * inv,
+                                  __uint_as_float(o[4 * v4 + 2]) * inv, __uint_as_float(o[4 * v4 + 3]) * inv);
+            if (full_tile) {
+              uint8_t* rowp = stg + (cb / 32) * 16384 + r * 128;
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
-            pkd[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
-          if (valid) {
+              for (int cc = 0; cc < 8; ++cc) *reinterpret_cast<float4*>(rowp + ((cc ^ (r & 7)) << 4)) = v[cc];
+            } else if (valid) {
+              float* O = static_cast<float*>(p.o) + (tok * p.Hq + h) * kD + cb;
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              reinterpret_cast<uint4*>(O)[v4] = make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
+              for (int v4 = 0; v4 < 8; ++v4) reinterpret_cast<float4*>(O)[v4] = v[v4];
+            }
+          } else {
+            uint32_t pkd[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+              pkd[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
+            if (full_tile) {
+              uint8_t* rowp = stg + (cb / 64) * 16384 + r * 128;
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc)
+                *reinterpret_cast<uint4*>(rowp + ((((cb % 64) / 8 + cc) ^ (r & 7)) << 4)) =
+                    make_uint4(pkd[4 * cc], pkd[4 * cc + 1], pkd[4 * cc + 2], pkd[4 * cc + 3]);
+            } else if (valid) {
+              __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o) + (tok * p.Hq + h) * kD + cb;
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4)
+                reinterpret_cast<uint4*>(O)[v4] = make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
+            }
           }
         }
+        if (valid)
+          p.lse[(long long)h * p.T + tok] = l > 0.f ? (m_ref + lg2_approx(l)) * kLn2 : -INFINITY;
       }
-      if (valid)
-        p.lse[(long long)h * p.T + tok] = l > 0.f ? (m_ref + lg2_approx(l)) * kLn2 : -INFINITY;
+      if (full_tile) {
+        // Every warp of the tile reaches this barrier (also after an abort);
+        // the stores go out only if all four staged their rows.
+        fence_proxy_async_smem();
+        const bool any_bad = named_bar_any(1 + t, 128, !ok);
+        if (!any_bad && q4 == 0 && lane == 0) {
+          const int boxes = (kD * esz) / 128;
+          for (int bx = 0; bx < boxes; ++bx)
+            tma_store_3d(&tmO, stg + bx * 16384, bx * (128 / esz), h, (int)(seq0 + m0 + 128 * t));
+          bulk_commit_group();
+          bulk_wait_group0();                  // shared memory must outlive the stores
+        }
+      }
     }
   }
 
@@ -484,9 +522,11 @@ int launch_impl(const AttnParams& p, cudaStream_t stream) {
   int r = make_tmap_u8_3d(&tq, p.q, kD, p.Hq, p.T, kD, (long long)kD * p.Hq, 128, 1, 128);
   if (!r) r = make_tmap_u8_3d(&tk, p.k, kD, p.Hkv, p.T, kD, (long long)kD * p.Hkv, 128, 1, 128);
   if (!r) r = make_tmap_u8_3d(&tv, p.v, p.vt_stride, kD, p.Hkv, p.vt_stride, p.vt_stride * kD, 128, 128, 1);
+  CUtensorMap to;
+  if (!r) r = p.o_f32 ? make_tmap_f32_3d(&to, p.o, kD, p.Hq, p.T, 128) : make_tmap_bf16_3d(&to, p.o, kD, p.Hq, p.T, 128);
   if (r) return r;
   dim3 grid((unsigned)(((p.N + 255) / 256) * p.Hq * p.B));
-  kern<<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  kern<<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(tq, tk, tv, to, p);
   return (int)cudaGetLastError();
 }
 

@@ -57,6 +57,19 @@ int make_tmap_bf16_3d_box(CUtensorMap* map, const void* base, int d, int H, long
   return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
 }
 
+int make_tmap_f32_3d(CUtensorMap* map, const void* base, int d, int H, long long T, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return (int)cudaErrorInitializationError;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)d * 4 * H};
+  cuuint32_t box[3] = {32, 1, (cuuint32_t)box_rows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
+}
+
 int make_tmap_u8_3d(CUtensorMap* map, const void* base, long long n0, long long n1, long long n2,
                     long long s1, long long s2, int b0, int b1, int b2) {
   EncodeTiledFn fn = encode_fn();

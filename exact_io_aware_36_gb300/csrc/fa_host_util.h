@@ -18,6 +18,10 @@ int make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int H, long lon
 int make_tmap_bf16_3d_box(CUtensorMap* map, const void* base, int d, int H, long long T,
                           int box_h, int box_t);
 
+// As make_tmap_bf16_3d over a float32 tensor [T, H, d], with a box of 32
+// columns (128 bytes) x 1 head x box_rows tokens.
+int make_tmap_f32_3d(CUtensorMap* map, const void* base, int d, int H, long long T, int box_rows);
+
 // Encodes a 3-D tiled TMA descriptor over a byte tensor (e4m3 codes) with
 // dims (innermost first) n0, n1, n2, byte strides s1 (of dim 1) and s2 (of
 // dim 2), box b0 x b1 x b2, 128-byte swizzle (b0 = 128), zero fill.  s1 and

@@ -213,6 +213,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, int
       : "memory");
 }
 
+// 3-D tiled store of a box from shared memory (bulk async-group).  The x
+// coordinate times the element size must be a multiple of 16 bytes, and no
+// coordinate may be negative.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+               :: "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // Element-wise fp32 add of `bytes` contiguous bytes from shared to global
 // memory (bulk async-group).  Both addresses 16-byte aligned, bytes % 16 == 0.
 __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, const void* ssrc, uint32_t bytes) {
