@@ -275,6 +275,10 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   } else {
     // ------------------------------------------------------------- softmax
     const int t = warp >> 2;
+    // this tile's step range as scalars (a runtime index into the arrays
+    // would put them in local memory)
+    const int nkv_t = t ? nkv[1] : nkv[0];
+    const int k0_t = t ? k0[1] : k0[0];
     const int q4 = warp & 3;
     const int rr = 32 * q4 + lane;                     // row within the tile
     const int row = m0 + 128 * t + rr;                 // row within the sequence
@@ -284,7 +288,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     uint8_t* prow = smem + C::P_OFF + t * C::TILE + rr * 128;
     const float vmax = __ldg(p.v_smax + kvh);
     // (a CTA without a second tile reads no scale for it)
-    const float sq = nkv[t] > 0 ? __ldg(p.q_scale + (long long)h * nbt + (long long)b * p.nblk + 2 * qb + t) : 1.f;
+    const float sq = nkv_t > 0 ? __ldg(p.q_scale + (long long)h * nbt + (long long)b * p.nblk + 2 * qb + t) : 1.f;
     const float c2q = p.scale_log2 * sq * (1.0f / kD);
     float slope2 = 0.f;
     if (ALIBI) slope2 = __ldg(p.alibi + h) * kLog2e;
@@ -292,7 +296,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     float l = 0.f;     // sum of P (exact): gives the LSE
     float lr = 0.f;    // sum of the rounded P / r: the weights the P V product used
     bool ok = true;
-    for (int j = 0; j < nkv[t]; ++j) {
+    for (int j = 0; j < nkv_t; ++j) {
       if (!(ok = wait_warp(&bars->s_full[t], j & 1, wc))) break;
       tc_fence_after();
       uint32_t s[128];
@@ -305,7 +309,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       reg_fence32(s + 32);
       reg_fence32(s + 64);
       reg_fence32(s + 96);
-      const int kt = kvj(k0[t] + j);
+      const int kt = kvj(k0_t + j);
       const int n0 = 128 * kt;
       const long long blk = (long long)kvh * nbt + (long long)b * p.nblk + kt;
       const float c2 = c2q * __ldg(p.k_scale + blk);
@@ -435,7 +439,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     // sequence is staged in the K/V slots in the TMA box layout and written
     // by TMA stores; a tile crossing the sequence end keeps per-thread
     // stores of its valid rows.
-    if (nkv[t] > 0) {                          // uniform over the tile's warps
+    if (nkv_t > 0) {                          // uniform over the tile's warps
       if (ok) ok = wait_warp(&bars->o_done, 0, wc);
       const bool full_tile = m0 + 128 * t + 128 <= L;
       const int r = 32 * q4 + lane;            // row within the tile
