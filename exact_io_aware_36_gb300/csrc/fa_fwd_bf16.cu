@@ -146,7 +146,26 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   auto kvj = [&](int k) { return REV ? hi[1] - k : lo[0] + k; };
   const int k0[2] = {REV ? hi[1] - hi[0] : 0, REV ? 0 : lo[1] - lo[0]};
 
-  if (threadIdx.x == 0) {
+  // The producer's lane initialises the barriers and starts the Q load and
+  // the first slots' K/V loads at once; the TMEM allocation and the CTA-wide
+  // sync run while those loads are in flight.
+  const int kvh = h / p.group;
+  auto issue_slot = [&](int j) {                // step j's slot: K_j and V_{j-1}
+    const int sl = j % C::NS;
+    const bool has_k = j < nkv_max, has_v = j >= 1;
+    mbar_arrive_expect_tx(&bars->kv_full[sl], (has_k + has_v) * C::TILE_BYTES);
+#pragma unroll
+    for (int bx = 0; bx < C::NB; ++bx) {
+      if (has_k)
+        tma_load_3d(smem + C::K_OFF + sl * C::TILE_BYTES + bx * C::BOX_BYTES, &tmK, bx * 64, kvh,
+                    (int)(seq0 + 128 * kvj(j)), &bars->kv_full[sl]);
+      if (has_v)
+        tma_load_3d(smem + C::V_OFF + sl * C::TILE_BYTES + bx * C::BOX_BYTES, &tmV, bx * 64, kvh,
+                    (int)(seq0 + 128 * kvj(j - 1)), &bars->kv_full[sl]);
+    }
+  };
+  const int early = min(C::NS, nkv_max + 1);    // slots filled before the sync
+  if (warp == kLoadWarp && lane == 0) {
     mbar_init(&bars->q_full, 1);
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
@@ -160,6 +179,17 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     mbar_init(&bars->o_done, 1);
     bars->abort_flag = 0;
     fence_mbarrier_init();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    const int ntiles = tile1 ? 2 : 1;
+    mbar_arrive_expect_tx(&bars->q_full, ntiles * C::TILE_BYTES);
+    for (int t = 0; t < ntiles; ++t)
+#pragma unroll
+      for (int bx = 0; bx < C::NB; ++bx)
+        tma_load_3d(smem + C::Q_OFF + t * C::TILE_BYTES + bx * C::BOX_BYTES, &tmQ, bx * 64, h,
+                    (int)(seq0 + m0 + 128 * t), &bars->q_full);
+    for (int j = 0; j < early; ++j) issue_slot(j);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(&bars->tmem_base, 512);
@@ -173,37 +203,11 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ producer
-    const int kvh = h / p.group;
-    if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      const int ntiles = tile1 ? 2 : 1;
-      mbar_arrive_expect_tx(&bars->q_full, ntiles * C::TILE_BYTES);
-      for (int t = 0; t < ntiles; ++t)
-#pragma unroll
-        for (int bx = 0; bx < C::NB; ++bx)
-          tma_load_3d(smem + C::Q_OFF + t * C::TILE_BYTES + bx * C::BOX_BYTES, &tmQ, bx * 64, h,
-                      (int)(seq0 + m0 + 128 * t), &bars->q_full);
-    }
-    __syncwarp();
-    int issued = 0;                   // slots whose loads were issued
-    for (int j = 0; j <= nkv_max; ++j) {      // j: step; its slot holds K_j and V_{j-1}
+    int issued = early;               // slots whose loads were issued
+    for (int j = early; j <= nkv_max; ++j) {
       const int sl = j % C::NS;
       if (!wait_warp(&bars->kv_empty[sl], ((j / C::NS) & 1) ^ 1, wc)) break;
-      if (lane == 0) {
-        const bool has_k = j < nkv_max, has_v = j >= 1;
-        mbar_arrive_expect_tx(&bars->kv_full[sl], (has_k + has_v) * C::TILE_BYTES);
-#pragma unroll
-        for (int bx = 0; bx < C::NB; ++bx) {
-          if (has_k)
-            tma_load_3d(smem + C::K_OFF + sl * C::TILE_BYTES + bx * C::BOX_BYTES, &tmK, bx * 64, kvh,
-                        (int)(seq0 + 128 * kvj(j)), &bars->kv_full[sl]);
-          if (has_v)
-            tma_load_3d(smem + C::V_OFF + sl * C::TILE_BYTES + bx * C::BOX_BYTES, &tmV, bx * 64, kvh,
-                        (int)(seq0 + 128 * kvj(j - 1)), &bars->kv_full[sl]);
-        }
-      }
+      if (lane == 0) issue_slot(j);
       __syncwarp();
       issued = j + 1;
     }
