@@ -21,7 +21,14 @@
 //     its transposed codes (128 head dims x 128 keys), so both products read
 //     K-major operands from shared memory;
 //   - P8 written by the softmax warps to shared memory (128 rows x 128 keys,
-//     swizzled) instead of TMEM, as the A operand of the PV product;
+//     swizzled, two buffers per tile) instead of TMEM, as the A operand of
+//     the PV product.  With P out of the S columns, S_t(j + 1) goes to the
+//     tensor cores as soon as the softmax has read S_t(j) (s_free), not after
+//     PV_t(j): the next scores are ready when the softmax finishes a tile, so
+//     the two tiles' softmax warps run back to back instead of waiting for
+//     PV + S each step.  P buffer b is reused two steps later, after
+//     PV_t(j - 2) is done (pv_done[t][b]); p_full is per buffer too, because
+//     the softmax can finish step j + 1 before PV_t(j) is issued;
 //   - 4 slots of 16 KB K and 16 KB V: slot j holds K_j and V_{j-1}, the
 //     operands of step j's products S_t(j) and PV_t(j-1), under one full and
 //     one empty barrier (one wait and one release per step for the MMA warp).
@@ -49,8 +56,8 @@ struct Cfg {
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + 2 * TILE;
   static constexpr int V_OFF = K_OFF + NS * TILE;
-  static constexpr int P_OFF = V_OFF + NS * TILE;
-  static constexpr int BAR_OFF = P_OFF + 2 * TILE;
+  static constexpr int P_OFF = V_OFF + NS * TILE;   // [tile][buffer] P codes
+  static constexpr int BAR_OFF = P_OFF + 4 * TILE;
   static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
   // The epilogue stages both tiles' O (fp32 at most) in the K/V slots.
   static_assert(2 * 128 * kD * 4 <= P_OFF - K_OFF, "O staging must fit the K/V slots");
@@ -61,7 +68,8 @@ struct Cfg {
 struct Bars {
   uint64_t q_full;
   uint64_t kv_full[8], kv_empty[8];
-  uint64_t s_full[2], p_full[2];
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full[2][2], pv_done[2][2];     // [tile][P buffer]
   uint64_t o_done;
   uint32_t tmem_base;
   int abort_flag;
@@ -174,7 +182,11 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_full[t], 4);
+      mbar_init(&bars->s_free[t], 4);
+      for (int bf = 0; bf < 2; ++bf) {
+        mbar_init(&bars->p_full[t][bf], 4);
+        mbar_init(&bars->pv_done[t][bf], 1);
+      }
     }
     mbar_init(&bars->o_done, 1);
     bars->abort_flag = 0;
@@ -241,26 +253,40 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       // TMA data needs no tcgen05 fence: the MMAs read it once the
       // transaction count of the slot's barrier has completed.
       if (!(ok = wait_warp(&bars->kv_full[sl], (j / C::NS) & 1, wc))) break;
+      // S_t(j) first, each once the softmax has read S_t(j - 1) ...
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
-        if (j >= 1 && j - 1 >= k0[t] && j - 1 < k0[t] + nkv[t]) {
-          if (!(ok = wait_warp(&bars->p_full[t], (j - 1 - k0[t]) & 1, wc))) break;
-          tc_fence_after();
-          if (lane == 0) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)             // 32 keys per MMA
-              mma_ss_f8(tmem + colO[t], desc_add(pdesc, t * C::TILE + kk * 32), desc_add(vdesc, kk * 32), IDESC,
-                        (j - 1 > k0[t] || kk > 0) ? 1u : 0u);
+        const int jl = j - k0[t];                      // tile t's local step
+        if (jl >= 0 && jl < nkv[t]) {
+          if (jl >= 1) {
+            if (!(ok = wait_warp(&bars->s_free[t], (jl - 1) & 1, wc))) break;
+            tc_fence_after();
           }
-          __syncwarp();
-        }
-        if (j >= k0[t] && j < k0[t] + nkv[t]) {
           if (lane == 0) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)             // 32 head dims per MMA
               mma_ss_f8(tmem + colS[t], desc_add(qdesc, t * C::TILE + kk * 32), desc_add(kdesc, kk * 32), IDESC,
                         kk > 0 ? 1u : 0u);
             mma_commit(&bars->s_full[t]);
+          }
+          __syncwarp();
+        }
+      }
+      if (!ok) break;
+      // ... then PV_t(j - 1) once its P is in shared memory
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int jl = j - 1 - k0[t];
+        if (jl >= 0 && jl < nkv[t]) {
+          const int bf = jl & 1;
+          if (!(ok = wait_warp(&bars->p_full[t][bf], (jl >> 1) & 1, wc))) break;
+          tc_fence_after();
+          if (lane == 0) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)             // 32 keys per MMA
+              mma_ss_f8(tmem + colO[t], desc_add(pdesc, (2 * t + bf) * C::TILE + kk * 32), desc_add(vdesc, kk * 32),
+                        IDESC, (jl > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&bars->pv_done[t][bf]);
           }
           __syncwarp();
         }
@@ -285,7 +311,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     const uint32_t lane_base = tmem + ((uint32_t)(32 * q4) << 16);
     const uint32_t tS = lane_base + (t ? C::S_COL1 : C::S_COL0);
     const uint32_t tO = lane_base + (t ? C::O_COL1 : C::O_COL0);
-    uint8_t* prow = smem + C::P_OFF + t * C::TILE + rr * 128;
+    uint8_t* prow0 = smem + C::P_OFF + 2 * t * C::TILE + rr * 128;   // buffer 0; buffer 1 is + TILE
     const float vmax = __ldg(p.v_smax + kvh);
     // (a CTA without a second tile reads no scale for it)
     const float sq = nkv_t > 0 ? __ldg(p.q_scale + (long long)h * nbt + (long long)b * p.nblk + 2 * qb + t) : 1.f;
@@ -309,6 +335,15 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       reg_fence32(s + 32);
       reg_fence32(s + 64);
       reg_fence32(s + 96);
+      // S_t(j) is in registers: the tensor cores may write S_t(j + 1)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->s_free[t]);
+      // P buffer j % 2 was last read by PV_t(j - 2)
+      uint8_t* prow = prow0 + (j & 1) * C::TILE;
+      if (j >= 2) {
+        if (!(ok = wait_warp(&bars->pv_done[t][j & 1], ((j - 2) >> 1) & 1, wc))) break;
+      }
       const int kt = kvj(k0_t + j);
       const int n0 = 128 * kt;
       const long long blk = (long long)kvh * nbt + (long long)b * p.nblk + kt;
@@ -412,6 +447,9 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         l *= alpha;
         lr *= alpha;
         if (j > 0 && __any_sync(0xffffffffu, raise)) {
+          // O must hold PV_t(j - 1) before it is rescaled
+          if (!(ok = wait_warp(&bars->pv_done[t][(j - 1) & 1], ((j - 1) >> 1) & 1, wc))) break;
+          tc_fence_after();
 #pragma unroll 1
           for (int cb = 0; cb < kD; cb += 16) {
             uint32_t o[16];
@@ -432,7 +470,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       fence_proxy_async_smem();                       // P codes visible to the tensor cores
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[t]);
+      if (lane == 0) mbar_arrive(&bars->p_full[t][j & 1]);
     }
     // ------------------------------------------------------------ epilogue
     // O and LSE as in the bf16 forward: a tile whose 128 rows all lie in the
