@@ -56,6 +56,17 @@ def test_fp32_shapes(causal, N, d, Hq, Hkv):
     check_full(x, O, lse, TOL_FP32, TOL_FP32)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp32_alibi_packed_odd_d(causal):
+    # packed lengths around the 32-key tile and the 4-row block (1, 3, 31..33,
+    # 100), GQA, ALiBi, and d = 37: rows and head columns with ragged tails
+    w = I.small_case("fp32", causal=causal, Hq=4, Hkv=2, d=37, alibi=True,
+                     seqlens=(1, 3, 31, 32, 33, 100), backward=False)
+    x = I.make_inputs(w, seed=12)
+    O, lse = G.forward(x)
+    check_full(x, O, lse, TOL_FP32, TOL_FP32)
+
+
 BF16_CASES = [
     # B, Hq, Hkv, N, d, causal, alibi
     (1, 1, 1, 128, 64, True, False),
