@@ -41,6 +41,7 @@ sys.path.insert(0, ROOT)
 from exact_io_aware_36_gb300 import inputs as I  # noqa: E402
 
 METRIC = "causal bf16 attention fwd+bwd TFLOP/s on 1 GB300; % of dense BF16 tensor peak"
+FWD_FP32_METRIC = "fp32 attention forward TFLOP/s on 1 GB300 (latency-bound size)"
 UNIT = "TFLOP/s"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_dram_traffic.json")
@@ -105,6 +106,21 @@ def load_peaks():
         return float(pk["bf16_tflops"]), float(pk.get("hbm_gbs", 0.0)), "measured"
     except Exception:
         return FALLBACK_BF16_TFLOPS, 6800.0, "fallback"
+
+
+def fp32_fma_peak_tflops(dev) -> float:
+    """fp32 FMA peak of the CUDA cores: SMs x 128 lanes x 2 flops x the
+    device's maximum SM clock."""
+    import torch
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    try:
+        out = subprocess.run(["nvidia-smi", "-i", str(smi_index(dev.index or 0)),
+                              "--query-gpu=clocks.max.sm", "--format=csv,noheader,nounits"],
+                             capture_output=True, text=True, timeout=10).stdout
+        mhz = float(out.strip().splitlines()[0])
+    except Exception:
+        mhz = 2070.0
+    return round(sms * 128 * 2 * mhz * 1e6 / 1e12, 2)
 
 
 def source_hash(name: str) -> str:
@@ -556,8 +572,16 @@ def run_ours(args, world, rank, local):
     fl = flops_per_step(w, x.seqlens)
     T = x.T
 
+    fp32 = w.dtype == "fp32"          # c1: fp32 operands, forward only
+    in_dtype = fa.FA_FP32 if fp32 else fa.FA_BF16
+
+    def host(name):
+        if fp32:
+            return torch.from_numpy(np.ascontiguousarray(getattr(x, name), dtype=np.float32))
+        return torch.from_numpy(x.bits[name].view("int16")).view(torch.bfloat16)
+
     def todev(name):
-        return torch.from_numpy(x.bits[name].view("int16")).view(torch.bfloat16).to(dev)
+        return host(name).to(dev)
 
     q, k, v = todev("q"), todev("k"), todev("v")
     do = todev("do") if w.backward else None
@@ -577,10 +601,10 @@ def run_ours(args, world, rank, local):
     det = 1 if args.deterministic else 0
     names = ["fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq" if det else "bwd_dq_convert"]
 
-    def step(evs=None):
+    def step(evs=None, ptrs=ptrs):
         if evs is not None:
             evs[0].record(stream)
-        st = fa.fa_fwd(ptrs[0], ptrs[1], ptrs[2], ptrs[3], ptrs[5], *common, fa.FA_BF16,
+        st = fa.fa_fwd(ptrs[0], ptrs[1], ptrs[2], ptrs[3], ptrs[5], *common, in_dtype,
                        fa.FA_FP32, sp)
         if st:
             raise fa.FAError(st, "fa_fwd")
@@ -651,7 +675,16 @@ def run_ours(args, world, rank, local):
         kern_flops = {"fwd": fl["fwd"], "bwd_dkdv": fl["bwd"]}
     dom = max(kern_ms, key=lambda n: kern_ms[n])
     peak, hbm, peak_src = load_peaks()
-    if dom in kern_flops:
+    if fp32:
+        # fp32 FMAs on the CUDA cores: 128 lanes x 2 flops per SM per clock
+        ach = kern_flops["fwd"] / (kern_ms["fwd"] * 1e-3) / 1e12
+        alu = fp32_fma_peak_tflops(dev)
+        roof = {"kernel": "fwd_fp32", "bound": "alu", "achieved": round(ach, 3), "peak": alu,
+                "unit": "TFLOP/s", "frac": round(ach / alu, 5),
+                "peak_source": "derived: SMs x 128 fp32 FMA lanes x 2 flops x max SM clock",
+                "note": "latency-bound at this size (one launch of a few microseconds)",
+                "traffic": None}
+    elif dom in kern_flops:
         ach = kern_flops[dom] / (kern_ms[dom] * 1e-3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": peak,
                 "unit": "TFLOP/s", "frac": round(ach / peak, 4),
@@ -669,27 +702,45 @@ def run_ours(args, world, rank, local):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, x, fl, world, dev, stream, step,
-                      [(q, "q"), (k, "k"), (v, "v")] + ([(do, "do")] if w.backward else []),
-                      [o, lse] + ([dq, dk, dv] if w.backward else []))
+        # two buffer sets: step i's kernels use set i % 2 while set (i+1) % 2
+        # takes the next step's inputs and gives back the previous outputs
+        in_names = ["q", "k", "v"] + (["do"] if w.backward else [])
+        sets = []
+        for b in range(2):
+            if b == 0:
+                bq, bk, bv, bo, bdo, blse, bdq, bdk, bdv = q, k, v, o, do, lse, dq, dk, dv
+            else:
+                bq, bk, bv, bo, blse = (torch.empty_like(t) for t in (q, k, v, o, lse))
+                bdo = torch.empty_like(do) if w.backward else None
+                bdq, bdk, bdv = (torch.empty_like(t) for t in (dq, dk, dv))
+            dev_in = [bq, bk, bv] + ([bdo] if w.backward else [])
+            sets.append({"ins": dev_in,
+                         "outs": [bo, blse] + ([bdq, bdk, bdv] if w.backward else []),
+                         "ptrs": (P(bq), P(bk), P(bv), P(bo), P(bdo), P(blse), P(bdq), P(bdk),
+                                  P(bdv))})
+        e2e = run_e2e(args, fl, world, dev, stream, step, [host(n) for n in in_names], sets,
+                      "fa_fwd + fa_bwd_stage x3" if w.backward else "fa_fwd")
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, x)
 
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "metric": FWD_FP32_METRIC if fp32 else METRIC, "value": round(value, 2 if not fp32 else 5),
+        "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if fp32 else "bf16",
         "data": "synthetic (seeded PCG64, seed 0; no dataset)",
         "config": {"workload": w.name, "desc": w.note, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
                    "N": w.N, "d": w.d, "causal": w.causal, "window": w.window,
                    "deterministic_bwd": bool(det),
                    "alibi": w.alibi, "varlen": w.varlen,
                    "total_tokens": T, "o_dtype": "fp32", "flops_per_step": fl["total"],
-                   "pct_of_peak": round(100.0 * value / world / peak, 2),
-                   "fwd_tflops": round(fwd_tflops, 1),
-                   "fwd_pct_of_peak": round(100.0 * fwd_tflops / peak, 2),
+                   "pct_of_peak": None if fp32 else round(100.0 * value / world / peak, 2),
+                   "fwd_tflops": round(fwd_tflops, 1 if not fp32 else 5),
+                   "fwd_pct_of_peak": None if fp32 else round(100.0 * fwd_tflops / peak, 2),
+                   "fwd_latency_us": round(kern_ms["fwd"] * 1e3, 2),
                    "l2": l2_note(w, T),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "per_kernel": per_kernel,
@@ -703,37 +754,66 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, w, x, fl, world, dev, stream, step, ins, outs):
+def run_e2e(args, fl, world, dev, stream, step, host_ins, sets, calls):
     """Same metric through the C ABI with host buffers: every step copies its
-    inputs from pinned host memory and its outputs back, inside the timing."""
+    inputs from pinned host memory and its outputs back to pinned host
+    memory, and all of those copies are inside the timed region.  The steps
+    are pipelined as a serving loop would run them: step i's kernels (on the
+    compute stream, buffer set i % 2) overlap the copy of step i+1's inputs
+    (copy-in stream) and of step i-1's outputs (copy-out stream).  A set is
+    refilled only after the kernels that read it are done, and overwritten
+    only after its outputs have been copied out."""
     import torch
-    hins = [(d, torch.from_numpy(x.bits[n].view("int16")).view(torch.bfloat16).pin_memory())
-            for d, n in ins]
-    houts = [(d, torch.empty(d.shape, dtype=d.dtype, pin_memory=True)) for d in outs]
-    h2d = sum(h.numel() * h.element_size() for _, h in hins)
-    d2h = sum(h.numel() * h.element_size() for _, h in houts)
+    hins = [h.pin_memory() for h in host_ins]
+    houts = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in sets[0]["outs"]]
+    h2d = sum(h.numel() * h.element_size() for h in hins)
+    d2h = sum(h.numel() * h.element_size() for h in houts)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    comp_done, out_done = [None, None], [None, None]
 
-    def e2e_step():
-        for d, h in hins:
-            d.copy_(h, non_blocking=True)
-        step()
-        for d, h in houts:
-            h.copy_(d, non_blocking=True)
+    def run(n):
+        for i in range(n):
+            b = i & 1
+            S = sets[b]
+            if comp_done[b] is not None:              # kernels of step i-2 read set b
+                s_in.wait_event(comp_done[b])
+            with torch.cuda.stream(s_in):
+                for d, h in zip(S["ins"], hins):
+                    d.copy_(h, non_blocking=True)
+            in_ev = torch.cuda.Event()
+            in_ev.record(s_in)
+            stream.wait_event(in_ev)
+            if out_done[b] is not None:               # outputs of step i-2 copied out
+                stream.wait_event(out_done[b])
+            step(None, S["ptrs"])
+            ce = torch.cuda.Event()
+            ce.record(stream)
+            comp_done[b] = ce
+            s_out.wait_event(ce)
+            with torch.cuda.stream(s_out):
+                for d, h in zip(S["outs"], houts):
+                    h.copy_(d, non_blocking=True)
+            oe = torch.cuda.Event()
+            oe.record(s_out)
+            out_done[b] = oe
 
-    for _ in range(2):
-        e2e_step()
+    run(2)
     torch.cuda.synchronize(dev)
     n = max(3, args.steps // 3)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(n):
-        e2e_step()
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    run(n)
+    stream.wait_event(out_done[(n - 1) & 1])       # the copy-out stream runs in order
     e1.record(stream)
     torch.cuda.synchronize(dev)
     ms = e0.elapsed_time(e1) / n
-    return {"value": round(world * fl["total"] / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
-            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "path": "fa_fwd + fa_bwd_stage x3 through the C ABI, pinned host buffers"}
+    return {"value": round(world * fl["total"] / (ms * 1e-3) / 1e12, 2 if fl["total"] > 1e9 else 5),
+            "unit": UNIT, "ms_per_step": round(ms, 3), "steps": n, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "path": calls + " through the C ABI; pinned host buffers; copies of step i+1's inputs "
+                    "and step i-1's outputs overlap step i's kernels (three streams, two buffer sets)"}
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -788,7 +868,8 @@ def run_reference(args, world, rank):
     else:
         w = I.workload(args.workload)
         x = I.make_inputs(w, seed=0)
-        sample_fn, metric, unit, scale = oracle_sample, METRIC, UNIT, 1e12
+        sample_fn, unit, scale = oracle_sample, UNIT, 1e12
+        metric = FWD_FP32_METRIC if w.dtype == "fp32" else METRIC
         shape = {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal,
                  "step": "one (sequence, head) sample of the workload per step"}
     for _ in range(max(args.warmup, 0)):
