@@ -487,16 +487,19 @@ def run_fp8(args, world, rank, local):
     sp = stream.cuda_stream
     P = lambda t: None if t is None else t.data_ptr()
 
-    def step(evs=None):
+    ptrs0 = (P(q), P(k), P(v), P(o), P(lse))
+
+    def step(evs=None, ptrs=ptrs0):
+        pq, pk, pv, po, plse = ptrs
         if evs is not None:
             evs[0].record(stream)
-        r = fa.fa_fp8_quantize(P(q), P(k), P(v), P(signs), w.B, w.Hq, w.Hkv, w.N, w.d, P(cu), T,
+        r = fa.fa_fp8_quantize(pq, pk, pv, P(signs), w.B, w.Hq, w.Hkv, w.N, w.d, P(cu), T,
                                P(buf), lay.total, sp)
         if r:
             raise fa.FAError(r, "fa_fp8_quantize")
         if evs is not None:
             evs[1].record(stream)
-        r = fa.fa_fwd_fp8(P(buf), lay.total, P(o), P(lse), w.B, w.Hq, w.Hkv, w.N, w.d,
+        r = fa.fa_fwd_fp8(P(buf), lay.total, po, plse, w.B, w.Hq, w.Hkv, w.N, w.d,
                           float(x.scale), int(w.causal), w.window_arg, P(cu), T, P(slopes),
                           fa.FA_FP32, sp)
         if r:
@@ -535,6 +538,17 @@ def run_fp8(args, world, rank, local):
     bf16_peak, _, src = load_peaks()
     peak = bf16_peak * FP8_OVER_BF16
     ach = fl / (a_ms * 1e-3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        # the quantized buffer is scratch of the compute stream: one suffices
+        sets = [{"ins": [q, k, v], "outs": [o, lse], "ptrs": ptrs0}]
+        q2, k2, v2, o2, lse2 = (torch.empty_like(t) for t in (q, k, v, o, lse))
+        sets.append({"ins": [q2, k2, v2], "outs": [o2, lse2],
+                     "ptrs": (P(q2), P(k2), P(v2), P(o2), P(lse2))})
+        host = lambda n: torch.from_numpy(x.bits[n].view("int16")).view(torch.bfloat16)
+        e2e = run_e2e(args, {"total": fl}, world, dev, stream, step,
+                      [host("q"), host("k"), host("v")], sets, "fa_fp8_quantize + fa_fwd_fp8")
     line = {
         "metric": FP8_METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
@@ -553,7 +567,9 @@ def run_fp8(args, world, rank, local):
                      "peak_source": f"{src} bf16 burst x {FP8_OVER_BF16:g} (nominal e4m3 / bf16 ratio)",
                      "traffic": ncu_traffic(w.name + " fp8", "fwd_fp8")},
         "gpu_launches": 4 * args.steps,
-        "clocks": clocks, "e2e": None, "cpu_baseline": None,
+        "clocks": clocks, "e2e": e2e,
+        "cpu_baseline": (oracle_fp8_baseline(w, x, I.hadamard_signs(w.d, seed=0))
+                         if rank == 0 and not args.no_cpu_baseline else None),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -847,6 +863,29 @@ def oracle_sample(w: I.Workload, x):
     dt = time.perf_counter() - t0
     flops = (14.0 if w.backward else 4.0) * w.d * pairs
     return flops, dt, what
+
+
+def oracle_fp8_baseline(w, x, signs):
+    """One whole (sequence, query head) of the workload through the FP8
+    oracle: transform, block quantization and attention on the dequantized
+    values, in fp64."""
+    from oracle import fp8 as F
+    s, e = int(x.cu_seqlens[0]), int(x.cu_seqlens[1])
+    L = e - s
+    cu = np.array([0, L], dtype=np.int64)
+    slopes = None if x.alibi_slopes is None else x.alibi_slopes[:1]
+    t0 = time.perf_counter()
+    qz = F.quantize_inputs(x.q[s:e, :1], x.k[s:e, :1], x.v[s:e, :1], signs, cu, L)
+    F.attention_forward_fp8(qz, cu, L, x.scale, w.causal, slopes, window=w.window)
+    dt = time.perf_counter() - t0
+    pairs = I.attended_pairs(dataclasses.replace(w, B=1, Hq=1, seqlens=None, seqlen_range=None),
+                             [L])
+    return {"value": round(4.0 * w.d * pairs / dt / 1e12, 6), "unit": UNIT,
+            "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"1 of {w.B * w.Hq} (sequence, query head) pairs: sequence 0 (L={L}), head 0",
+            "seconds": round(dt, 2),
+            "note": "NumPy: float32 transform and e4m3 codes, float64 attention on the "
+                    "dequantized values; BLAS threads = all cores"}
 
 
 def cpu_baseline(w, x):
