@@ -108,19 +108,53 @@ def load_peaks():
         return FALLBACK_BF16_TFLOPS, 6800.0, "fallback"
 
 
+def max_sm_mhz(dev) -> float:
+    try:
+        out = subprocess.run(["nvidia-smi", "-i", str(smi_index(dev.index or 0)),
+                              "--query-gpu=clocks.max.sm", "--format=csv,noheader,nounits"],
+                             capture_output=True, text=True, timeout=10).stdout
+        return float(out.strip().splitlines()[0])
+    except Exception:
+        return 2070.0
+
+
 def fp32_fma_peak_tflops(dev) -> float:
     """fp32 FMA peak of the CUDA cores: SMs x 128 lanes x 2 flops x the
     device's maximum SM clock."""
     import torch
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    try:
-        out = subprocess.run(["nvidia-smi", "-i", str(smi_index(dev.index or 0)),
-                              "--query-gpu=clocks.max.sm", "--format=csv,noheader,nounits"],
-                             capture_output=True, text=True, timeout=10).stdout
-        mhz = float(out.strip().splitlines()[0])
-    except Exception:
-        mhz = 2070.0
-    return round(sms * 128 * 2 * mhz * 1e6 / 1e12, 2)
+    return round(sms * 128 * 2 * max_sm_mhz(dev) * 1e6 / 1e12, 2)
+
+
+# ex2.approx.ftz.f32 per SM per clock, measured on GB300 by tests/probes/alu_rate.cu
+EX2_PER_SM_CLK = 30.3
+
+
+def secondary_roofs(w, T, fl, kern_ms, dev, hbm_gbs, det=False):
+    """The exp2 (MUFU) and HBM roofs of the forward and dK/dV kernels beside
+    their tensor roof: one exp2 per attended pair in each, and the bytes each
+    must move at least (inputs read once, outputs written once; dK/dV also
+    reads and writes the fp32 dQ accumulator once, except in the
+    deterministic backward, which has none)."""
+    import torch
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ex2_peak = sms * EX2_PER_SM_CLK * max_sm_mhz(dev) * 1e6          # exp2 per second
+    qb, kvb = T * w.Hq * w.d, T * w.Hkv * w.d                        # elements
+    alg = {"fwd": 2 * qb + 2 * 2 * kvb + 4 * qb + 4 * w.Hq * T,        # q, k, v in; O fp32, LSE out
+           "bwd_dkdv": (2 * qb + 2 * 2 * kvb + 2 * qb + 2 * 4 * w.Hq * T  # q, k, v, dO, LSE, D in
+                        + 2 * 2 * kvb + (0 if det else 2 * 4 * qb))}   # dK, dV out; dQacc in and out
+    out = {}
+    for n in ("fwd", "bwd_dkdv"):
+        if n not in kern_ms or (n == "bwd_dkdv" and not w.backward):
+            continue
+        sec = kern_ms[n] * 1e-3
+        ex2_rate = fl["pairs"] / sec
+        gbs = alg[n] / sec / 1e9
+        out[n] = {"exp2_per_s": float(f"{ex2_rate:.4g}"), "exp2_peak_per_s": float(f"{ex2_peak:.4g}"),
+                  "exp2_frac": round(ex2_rate / ex2_peak, 4),
+                  "alg_bytes": int(alg[n]), "hbm_gbs": round(gbs, 1),
+                  "hbm_frac": round(gbs / hbm_gbs, 4) if hbm_gbs else None}
+    return out
 
 
 def source_hash(name: str) -> str:
@@ -761,6 +795,7 @@ def run_ours(args, world, rank, local):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "per_kernel": per_kernel,
         "roofline": roof,
+        "secondary_roofs": None if fp32 else secondary_roofs(w, T, fl, kern_ms, dev, hbm, bool(det)),
         "gpu_launches": args.steps * (4 if w.backward else 1),
         "clocks": clocks,
         "e2e": e2e,
