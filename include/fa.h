@@ -150,6 +150,12 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
  *                      and D, one query tile per block)
  * The same checks as fa_bwd run first; an unknown stage is
  * FA_ERR_UNSUPPORTED.
+ * FA_BWD_DKDV hands out its work items from a counter in the workspace that
+ * must read zero when it starts: FA_BWD_PREPROCESS zeroes it, and each
+ * FA_BWD_DKDV that completes sets it back to zero.  So on a fresh workspace
+ * (or after a call that ended in FA_ERR_DEVICE_TIMEOUT) run
+ * FA_BWD_PREPROCESS before FA_BWD_DKDV; repeating FA_BWD_DKDV alone on a
+ * workspace is otherwise allowed.
  */
 typedef enum { FA_BWD_PREPROCESS = 0, FA_BWD_DKDV = 1, FA_BWD_DQ_CONVERT = 2 } fa_bwd_stage_id;
 
