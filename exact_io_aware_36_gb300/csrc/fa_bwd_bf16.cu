@@ -332,6 +332,10 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       if (lane == 0) {
         while (true) {
           w = atomicAdd(p.work_ctr, 1);
+          if (w < 0) {                     // counter never zeroed: no item is trusted
+            record_status(p.status, FA_ERR_WORKSPACE);
+            w = nwork;
+          }
           if (w >= nwork) break;
           if (!dkdv_item<CAUSAL, BAND>(p, w, it)) { record_status(p.status, FA_ERR_CU_SEQLENS); continue; }
           if (it.n0 < it.L) break;

@@ -155,7 +155,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
  * FA_BWD_DKDV that completes sets it back to zero.  So on a fresh workspace
  * (or after a call that ended in FA_ERR_DEVICE_TIMEOUT) run
  * FA_BWD_PREPROCESS before FA_BWD_DKDV; repeating FA_BWD_DKDV alone on a
- * workspace is otherwise allowed.
+ * workspace is otherwise allowed.  A negative counter found on the device
+ * ends the stage's work and sets FA_ERR_WORKSPACE in the status word.
  */
 typedef enum { FA_BWD_PREPROCESS = 0, FA_BWD_DKDV = 1, FA_BWD_DQ_CONVERT = 2 } fa_bwd_stage_id;
 

@@ -87,3 +87,46 @@ def test_repeated_dkdv_stage_recomputes_every_item(deterministic):
     assert t.equal(dk, dk1) and t.equal(dv, dv1)
     _, _, _, dk_r, dv_r = G.backward(x, deterministic=bool(deterministic))
     assert np.array_equal(G.as_f64(dk), dk_r) and np.array_equal(G.as_f64(dv), dv_r)
+
+
+def test_dkdv_stage_with_a_negative_counter_reports_and_recovers():
+    # A workspace whose item counter was never zeroed (here: -1000) must not
+    # turn into negative item indices: the stage does no work, sets
+    # FA_ERR_WORKSPACE, and puts the counter back to zero, so the next launch
+    # computes every item.
+    t = G.torch()
+    w = I.small_case("bf16", causal=True, B=1, Hq=4, Hkv=2, N=700, d=128)
+    x = I.make_inputs(w, seed=74)
+    q, k, v, do = (G.to_dev(x, n) for n in ("q", "k", "v", "do"))
+    o, lse = fa.attention_forward(q, k, v, causal=True, scale=x.scale, batch=w.B,
+                                  out_dtype=t.float32, check=True)
+    T, H, Hkv, d = w.B * w.N, w.Hq, w.Hkv, w.d
+    dq, dk, dv = t.empty_like(q), t.empty_like(k), t.empty_like(v)
+    wsb = fa.fa_bwd_workspace_size(w.B, H, w.N, d, 0)
+    ws = t.empty(wsb, dtype=t.uint8, device="cuda")
+    r256 = lambda n: (n + 255) // 256 * 256
+    ctr = ws[r256(H * T * 4) + r256(H * T * d * 4):].view(t.int32)
+    p = lambda a: a.data_ptr()
+    stream = t.cuda.current_stream().cuda_stream
+
+    def stage(s):
+        st = fa.fa_bwd_stage(s, p(q), p(k), p(v), p(o), p(do), p(lse), p(dq), p(dk), p(dv), w.B, H,
+                             Hkv, w.N, d, x.scale, True, -1, None, 0, None, fa.FA_BF16, fa.FA_FP32,
+                             0, p(ws), wsb, stream)
+        assert st == 0, fa.fa_status_string(st)
+
+    stage(0)
+    ctr[0] = -1000
+    ctr[1] = 0
+    stage(1)
+    t.cuda.synchronize()
+    assert fa.STATUS[fa.fa_check_device_error(None)] == "FA_ERR_WORKSPACE"
+    assert int(ctr[0]) == 0 and int(ctr[1]) == 0
+    stage(1)
+    stage(2)
+    t.cuda.synchronize()
+    assert fa.fa_check_device_error(None) == 0
+    _, _, dq_r, dk_r, dv_r = G.backward(x)
+    assert np.array_equal(G.as_f64(dk), dk_r) and np.array_equal(G.as_f64(dv), dv_r)
+    err = np.abs(G.as_f64(dq) - dq_r).max() / max(np.abs(dq_r).max(), 1e-3)
+    assert err <= 1e-2, err
