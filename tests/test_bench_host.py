@@ -53,3 +53,25 @@ def test_reference_arm_line_for_the_fp32_workload():
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert np.isfinite(line["value"]) and line["value"] > 0
+
+
+def test_secondary_roofs_algorithmic_bytes(monkeypatch):
+    # c3: the forward reads q, k, v (bf16) and writes O (fp32) and LSE:
+    # 403 MB + 270 MB; dK/dV reads q, k, v, dO, LSE, D and the fp32 dQ
+    # accumulator and writes dK, dV and the accumulator: 810 MB + 537 MB.
+    import types
+    import torch
+    monkeypatch.setattr(torch.cuda, "get_device_properties",
+                        lambda dev: types.SimpleNamespace(multi_processor_count=152))
+    monkeypatch.setattr(bench, "max_sm_mhz", lambda dev: 2070.0)
+    w = I.workload("c3_long")
+    T = w.B * w.N
+    fl = bench.flops_per_step(w, [w.N] * w.B)
+    out = bench.secondary_roofs(w, T, fl, {"fwd": 1.0, "bwd_dkdv": 2.0}, "cpu", 6796.9)
+    assert out["fwd"]["alg_bytes"] == 402_653_184 + 270_532_608
+    assert out["bwd_dkdv"]["alg_bytes"] == 809_500_672 + 536_870_912
+    # one exp2 per attended pair; peak 152 x 30.3 x 2.07 GHz
+    assert abs(out["fwd"]["exp2_per_s"] / (fl["pairs"] / 1e-3) - 1) < 1e-3
+    assert abs(out["fwd"]["exp2_peak_per_s"] / (152 * 30.3 * 2070e6) - 1) < 1e-3
+    det = bench.secondary_roofs(w, T, fl, {"fwd": 1.0, "bwd_dkdv": 2.0}, "cpu", 6796.9, det=True)
+    assert det["bwd_dkdv"]["alg_bytes"] == out["bwd_dkdv"]["alg_bytes"] - 2 * 4 * T * w.Hq * w.d
