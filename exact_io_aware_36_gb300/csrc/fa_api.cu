@@ -143,6 +143,33 @@ size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, long long total_tokens
   return round256((size_t)Hq * T * sizeof(float)) + round256((size_t)Hq * T * d * sizeof(float)) + 256;
 }
 
+}  // extern "C"
+
+namespace fa {
+
+fa_status bwd_check_args(const void* q, const void* k, const void* v, const void* o,
+                         const void* dO, const float* lse, const void* dq, const void* dk,
+                         const void* dv, int B, int Hq, int Hkv, int N, int d, float scale,
+                         int causal, int window, const int32_t* cu_seqlens,
+                         long long total_tokens, fa_dtype dtype, fa_dtype o_dtype,
+                         int deterministic, long long* T) {
+  fa_status st = check_sizes(B, Hq, Hkv, N, d, scale, cu_seqlens, total_tokens, dtype, true, T);
+  if (st != FA_OK) return st;
+  if (o_dtype != FA_FP32 && o_dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+  if (window >= 0 && !causal) return FA_ERR_UNSUPPORTED;
+  if (deterministic != 0 && deterministic != 1) return FA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(lse))
+    return FA_ERR_ALIGN;
+  if (B == 0 || N == 0) *T = 0;
+  return FA_OK;
+}
+
+}  // namespace fa
+
+extern "C" {
+
 static fa_status bwd_impl(int stage, const void* q, const void* k, const void* v, const void* o,
                           const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
                           int Hq, int Hkv, int N, int d, float scale, int causal, int window,
@@ -150,18 +177,13 @@ static fa_status bwd_impl(int stage, const void* q, const void* k, const void* v
                           const float* alibi_slopes, fa_dtype dtype, fa_dtype o_dtype,
                           int deterministic, void* workspace, size_t workspace_bytes,
                           void* stream) {
-  long long T = 0;
-  fa_status st = check_sizes(B, Hq, Hkv, N, d, scale, cu_seqlens, total_tokens, dtype, true, &T);
-  if (st != FA_OK) return st;
-  if (o_dtype != FA_FP32 && o_dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
-  if (window >= 0 && !causal) return FA_ERR_UNSUPPORTED;
-  if (deterministic != 0 && deterministic != 1) return FA_ERR_UNSUPPORTED;
   if (stage < -1 || stage > 2) return FA_ERR_UNSUPPORTED;
-  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
-      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(lse))
-    return FA_ERR_ALIGN;
-  if (T == 0 || B == 0 || N == 0) return FA_OK;
+  long long T = 0;
+  fa_status st = fa::bwd_check_args(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale,
+                                    causal, window, cu_seqlens, total_tokens, dtype, o_dtype,
+                                    deterministic, &T);
+  if (st != FA_OK) return st;
+  if (T == 0) return FA_OK;
   const size_t need = fa_bwd_workspace_size(B, Hq, N, d, T);
   if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_ALIGN;

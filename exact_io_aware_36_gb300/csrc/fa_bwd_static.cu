@@ -10,11 +10,16 @@
 // For them, fa_bwd_static_scratch runs the same three backward kernels with
 // the workspace placed in a fixed array in the library's own device memory.
 //
-// The array is a file-scope __device__ variable: every GPU that loads the
-// library holds FA_BWD_STATIC_SCRATCH_BYTES for it until the process exits.
-// In host code its name is only a host-side stand-in, so the device address
-// is looked up once per device with cudaGetSymbolAddress and passed to the
-// kernels like any caller-owned workspace.
+// The array is a file-scope __device__ variable: once reserved on a GPU it
+// stays until the process exits.  When it is reserved depends on how CUDA
+// loads modules: eagerly, with the library's module; under lazy loading
+// (CUDA_MODULE_LOADING=LAZY, the default since CUDA 12.2) only when this
+// file's module is first needed, which is the first call's
+// cudaGetSymbolAddress below.  So the first call on each device may itself
+// reserve the 64 MiB.  In host code the array's name is only a host-side
+// stand-in, so the device address is looked up once per device with
+// cudaGetSymbolAddress and passed to the kernels like any caller-owned
+// workspace.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -51,9 +56,16 @@ extern "C" fa_status fa_bwd_static_scratch(
     void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, float scale, int causal,
     int window, const int32_t* cu_seqlens, long long total_tokens, const float* alibi_slopes,
     fa_dtype dtype, fa_dtype o_dtype, int deterministic, void* stream) {
-  // The size check comes first and needs no GPU: a problem whose D and dQ
-  // accumulator do not fit the fixed array is refused before anything runs.
-  const long long T = cu_seqlens ? total_tokens : (long long)B * N;
+  // fa_bwd's own argument checks come first, so a bad argument gets the same
+  // status as from fa_bwd, and an empty problem (no tokens) succeeds without
+  // touching the GPU whatever its nominal sizes.  The size check follows; it
+  // needs no GPU either: a problem whose D and dQ accumulator do not fit the
+  // fixed array is refused before anything runs.
+  long long T = 0;
+  const fa_status st = fa::bwd_check_args(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d,
+                                          scale, causal, window, cu_seqlens, total_tokens, dtype,
+                                          o_dtype, deterministic, &T);
+  if (st != FA_OK || T == 0) return st;
   const size_t need = fa_bwd_workspace_size(B, Hq, N, d, T);
   if (need > (size_t)FA_BWD_STATIC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
   void* ws = scratch_ptr();

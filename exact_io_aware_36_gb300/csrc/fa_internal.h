@@ -115,6 +115,16 @@ inline int decode_chunk(int B, int Hkv, int S_max) {
   return c;
 }
 
+// The host-side argument checks of fa_bwd (everything but the workspace), in
+// fa_bwd's order.  On FA_OK, *T is the total token count, or 0 when the call
+// has nothing to compute.
+fa_status bwd_check_args(const void* q, const void* k, const void* v, const void* o,
+                         const void* dO, const float* lse, const void* dq, const void* dk,
+                         const void* dv, int B, int Hq, int Hkv, int N, int d, float scale,
+                         int causal, int window, const int32_t* cu_seqlens,
+                         long long total_tokens, fa_dtype dtype, fa_dtype o_dtype,
+                         int deterministic, long long* T);
+
 // Launchers (each returns a cudaError_t value as int).
 int launch_fwd_fp32(const AttnParams& p, void* stream);
 int launch_fwd_bf16(const AttnParams& p, void* stream);

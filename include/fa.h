@@ -104,9 +104,12 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  void* stream);
 
 /*
- * Bytes of device workspace fa_bwd needs: D (float32 [Hq, T]), the dQ
- * accumulator (float32 [Hq, T, d]) and 256 bytes for the dK/dV kernel's
- * work-item counter, each part 256-byte aligned.  T is total_tokens when
+ * Bytes of device workspace fa_bwd needs: D (float32 [Hq, T]; the row-dot
+ * D_i = dO_i . O_i of "FlashAttention: Faster Attention Without Dropping a
+ * Single Interaction", Key design 3), the dQ accumulator (float32
+ * [Hq, T, d]; the same design's dQ += dS K summed over key tiles) and 256
+ * bytes for the dK/dV kernel's work-item counter, each part 256-byte
+ * aligned.  T is total_tokens when
  * > 0, else B*N.  Returns 0 for invalid sizes.  The deterministic backward
  * does not use the accumulator; this size serves both.
  */
@@ -182,16 +185,23 @@ fa_status fa_bwd_stage(int stage, const void* q, const void* k, const void* v, c
  * array of FA_BWD_STATIC_SCRATCH_BYTES inside the library's device memory.
  * It calls no cudaMalloc, cudaFree or other allocating routine.
  *
- * - Limit: a problem needing more than FA_BWD_STATIC_SCRATCH_BYTES of
- *   workspace (fa_bwd_workspace_size) is refused with FA_ERR_WORKSPACE
- *   before anything is launched.  64 MiB holds about 130,000 (token,
+ * - Limit: fa_bwd's argument checks run first (same status codes); then a
+ *   problem needing more than FA_BWD_STATIC_SCRATCH_BYTES of workspace
+ *   (fa_bwd_workspace_size) is refused with FA_ERR_WORKSPACE before
+ *   anything is launched.  64 MiB holds about 130,000 (token,
  *   query head) rows at d = 128 and 258,000 at d = 64, e.g. B = 8, H = 16,
  *   N = 1024, d = 64 (34 MB).
- * - Memory: every GPU that loads the library holds the array until the
- *   process exits, whether or not this entry point is used.
+ * - Memory: the array, once reserved on a GPU, stays until the process
+ *   exits.  With CUDA's lazy module loading (CUDA_MODULE_LOADING=LAZY, the
+ *   default since CUDA 12.2) it is reserved only when the first call on that
+ *   device looks it up, so that first call may itself take 64 MiB of device
+ *   memory; with eager loading it is reserved when the library's module is
+ *   loaded, whether or not this entry point is used.
  * - Set-up: the first call with a given device current looks up the
- *   array's device address (cudaGetSymbolAddress) and caches it; make that
- *   first call before any stream capture on that device.
+ *   array's device address (cudaGetSymbolAddress) and caches it.  Make that
+ *   first call at start-up: before the caller's runtime fixes its device
+ *   memory, and before any stream capture on that device.  A call with no
+ *   tokens to process returns FA_OK without this set-up.
  * - Sharing: all calls on a device use the same array and it keeps the last
  *   call's contents.  Each call rewrites everything it reads (D, and a
  *   zeroed dQ accumulator), but calls that overlap on the GPU (different
@@ -294,6 +304,8 @@ fa_status fa_fwd_fp8(const void* fp8_buf, size_t fp8_bytes, void* o, float* lse,
                      const float* alibi_slopes, fa_dtype o_dtype, void* stream);
 
 /*
+ * Error reporting of this library (the pages have no counterpart; their
+ * usage contract only names the inputs a call takes).
  * Synchronises `stream`, then reads and clears the current device's status
  * word.  Returns FA_OK, FA_ERR_DEVICE_TIMEOUT, FA_ERR_CU_SEQLENS, or
  * FA_ERR_CUDA if the synchronisation itself failed.
@@ -311,7 +323,8 @@ fa_status fa_check_device_error(void* stream);
  */
 fa_status fa_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
 
-/* Static description of a status code (never NULL). */
+/* Static description of a status code (never NULL); part of this library's
+ * error reporting, with no counterpart on the pages. */
 const char* fa_status_string(fa_status status);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
