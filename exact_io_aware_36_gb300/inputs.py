@@ -37,7 +37,7 @@ __all__ = [
     "Workload", "WORKLOADS", "EXTRA_WORKLOADS", "workload", "make_inputs", "small_case",
     "bf16_round", "bf16_bits", "bf16_from_bits", "alibi_slopes",
     "attended_pairs", "DecodeWorkload", "DECODE_WORKLOADS", "DecodeInputs",
-    "make_decode_inputs", "decode_bytes", "hadamard_signs",
+    "make_decode_inputs", "decode_bytes", "hadamard_signs", "add_score_structure",
 ]
 
 
@@ -231,6 +231,70 @@ def make_inputs(w: Workload, seed: int = 0, with_do: Optional[bool] = None) -> I
             x[...] = bf16_from_bits(b)
     slopes = alibi_slopes(w.Hq) if w.alibi else None
     return Inputs(w, seed, L, cu.astype(np.int32), q, k, v, do, slopes, w.scale, bits)
+
+
+# Dominant keys of the "late_dominant" structure: offsets within each
+# sequence (the second, fourth and sixth 128-key tiles) and the score each
+# adds, as a multiple of the structure's strength.
+_DOMINANT_AT = ((128 + 37, 1.0), (384 + 5, 2.0), (640 + 90, 3.0))
+
+
+def add_score_structure(x: Inputs, kind: str, strength: float, seed: int = 0) -> Inputs:
+    """Overlay a peaked or drifting score pattern on drawn inputs, in place.
+
+    The softmax regimes these produce are the ones where the running maximum
+    of a row changes by many nats between key tiles.  One direction u_g per
+    kv head is drawn (``standard_normal``, rescaled to |u_g|^2 = d) from a
+    fresh PCG64(seed) generator; every query row of a head of g's group gets
+    + u_g, and keys get + c u_g, which adds c * scale * d to their scores
+    against every query row (c is chosen so that this is ``strength`` nats
+    times the pattern's profile):
+
+    * ``"late_dominant"``: the keys at offsets 165, 389 and 730 of each
+      sequence (second, fourth and sixth 128-key tile, where the sequence is
+      long enough) get 1, 2 and 3 x strength: rows past them see their
+      maximum jump up at those tiles.
+    * ``"rising"``: key j of a sequence of length L gets strength * j / L.
+    * ``"falling"``: key j gets strength * (1 - j / L).
+
+    q and k are then rounded to the storage type again (bf16 workloads keep
+    their bit patterns in ``x.bits``).  Nothing of the attention arithmetic
+    is computed here: the pattern is an input.
+    """
+    w = x.workload
+    rng = np.random.Generator(np.random.PCG64(seed))
+    u = rng.standard_normal(size=(w.Hkv, w.d)).astype(np.float64)
+    u *= np.sqrt(w.d) / np.linalg.norm(u, axis=1, keepdims=True)
+    group = w.Hq // w.Hkv
+    unit = 1.0 / (x.scale * w.d)          # key coefficient that adds one nat
+    q = x.q.astype(np.float64)
+    k = x.k.astype(np.float64)
+    q += np.repeat(u, group, axis=0)[None, :, :]
+    cu = x.cu_seqlens.astype(np.int64)
+    for b in range(len(cu) - 1):
+        s, e = int(cu[b]), int(cu[b + 1])
+        L = e - s
+        if L == 0:
+            continue
+        if kind == "late_dominant":
+            prof = np.zeros(L)
+            for off, mult in _DOMINANT_AT:
+                if off < L:
+                    prof[off] = mult
+        elif kind == "rising":
+            prof = np.arange(L) / L
+        elif kind == "falling":
+            prof = 1.0 - np.arange(L) / L
+        else:
+            raise ValueError(f"unknown structure {kind!r}")
+        k[s:e] += (strength * unit * prof)[:, None, None] * u[None, :, :]
+    for name, arr in (("q", q), ("k", k)):
+        f32 = arr.astype(np.float32)
+        if w.dtype == "bf16":
+            x.bits[name] = bf16_bits(f32)
+            f32 = bf16_from_bits(x.bits[name])
+        getattr(x, name)[...] = f32
+    return x
 
 
 def with_seqlens(w: Workload, seqlens) -> Workload:

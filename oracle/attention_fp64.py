@@ -60,7 +60,7 @@ __all__ = [
     "attention_forward", "attention_backward", "head_forward", "head_backward",
     "head_scores", "online_softmax_forward", "online_softmax_forward_normalised",
     "forward_rows", "backward_query_rows", "backward_key_rows", "head_row_stats",
-    "decode_forward",
+    "decode_forward", "head_forward_chunked", "head_backward_chunked",
 ]
 
 
@@ -452,6 +452,77 @@ def backward_key_rows(q, k, v, do, scale, causal, rows, cu_seqlens=None,
         outK.append(dk)
         outV.append(dv)
     return np.array(outK), np.array(outV)
+
+
+# --------------------------------------------------------------------------
+# Whole heads of long sequences, by blocks of query rows.  Rows of S and P
+# are independent of each other, so each block of rows is Key design 1 / 3
+# applied to those rows; the sums over rows that make dK and dV are added
+# block by block.  Only the memory held at once changes, not the arithmetic
+# of any entry.
+# --------------------------------------------------------------------------
+
+def _score_rows(q_rows, k, scale, causal, r0, slope=None, window=None):
+    """Rows r0 .. r0 + len(q_rows) - 1 of ``head_scores`` (same definition:
+    scale q k^T, R4's bias -slope (i - j), R6's causal mask and R9's band)."""
+    window = _window(window, causal)
+    S = scale * (_f64(q_rows) @ _f64(k).T)
+    i = np.arange(r0, r0 + S.shape[0], dtype=np.float64)[:, None]
+    j = np.arange(S.shape[1], dtype=np.float64)[None, :]
+    if slope is not None:
+        S = S - float(slope) * (i - j)
+    if causal:
+        vis = j <= i
+        if window is not None:
+            vis &= j >= i - window
+        S = np.where(vis, S, -np.inf)
+    return S
+
+
+def head_forward_chunked(q, k, v, scale, causal, slope=None, window=None, chunk=1024):
+    """O and LSE of one (sequence, head), ``chunk`` query rows at a time.
+
+    [FA1 note] Key design 1 for each block of rows: S rows, P = softmax(S)
+    row-wise, O = P V, and L = m + log l (Key design 2's table, R3)."""
+    L = q.shape[0]
+    vv = _f64(v)
+    O = np.empty((L, vv.shape[1]))
+    lse = np.empty(L)
+    for r0 in range(0, L, chunk):
+        r1 = min(r0 + chunk, L)
+        P, lse[r0:r1] = _softmax_rows(_score_rows(q[r0:r1], k, scale, causal, r0, slope, window))
+        O[r0:r1] = P @ vv
+    return O, lse
+
+
+def head_backward_chunked(q, k, v, do, scale, causal, slope=None, window=None, chunk=1024):
+    """dQ, dK, dV, O, LSE and D of one (sequence, head), ``chunk`` query rows
+    at a time.
+
+    [FA1 note] Key design 3 for each block of rows: P from the rows' scores,
+    dP = dO V^T, D = rowsum(P o dP), dS = P o (dP - D), dQ = scale dS K (R2)
+    for those rows; dV = P^T dO and dK = scale dS^T Q summed over the blocks.
+    Same results as ``head_backward`` without holding the whole L x L
+    matrices.  Returns (dQ, dK, dV, O, LSE, D)."""
+    L = q.shape[0]
+    qq, kk, vv, dd = _f64(q), _f64(k), _f64(v), _f64(do)
+    dQ = np.empty(qq.shape)
+    dK = np.zeros(kk.shape)
+    dV = np.zeros(vv.shape)
+    O = np.empty((L, vv.shape[1]))
+    lse = np.empty(L)
+    D = np.empty(L)
+    for r0 in range(0, L, chunk):
+        r1 = min(r0 + chunk, L)
+        P, lse[r0:r1] = _softmax_rows(_score_rows(qq[r0:r1], kk, scale, causal, r0, slope, window))
+        O[r0:r1] = P @ vv
+        dP = dd[r0:r1] @ vv.T
+        D[r0:r1] = (P * dP).sum(axis=1)
+        dS = P * (dP - D[r0:r1, None])
+        dQ[r0:r1] = scale * (dS @ kk)
+        dK += scale * (dS.T @ qq[r0:r1])
+        dV += P.T @ dd[r0:r1]
+    return dQ, dK, dV, O, lse, D
 
 
 # --------------------------------------------------------------------------

@@ -314,6 +314,51 @@ def test_sampled_rows_equal_full_oracle():
         np.testing.assert_allclose(dv_r[n], dv[t, g], atol=1e-12)
 
 
+# ----------------------------------------------------- whole-head row blocks
+
+@pytest.mark.parametrize("causal,slope,window", [(False, None, None), (True, None, None),
+                                                 (True, 0.37, None), (True, None, 5),
+                                                 (False, 0.2, None)])
+@pytest.mark.parametrize("chunk", [1, 3, 7, 40])
+def test_chunked_head_forms_equal_the_whole_matrices(causal, slope, window, chunk):
+    """The row-block forms used for whole heads of long sequences give the
+    whole-matrix oracle's O, LSE, D and gradients (to 1e-12): a block that
+    is dropped, mis-offset (the causal mask, the band and the ALiBi index
+    use the block's first row) or overwritten instead of summed fails."""
+    L, d = 29, 6
+    q, k, v, do = rnd(90, L, d), rnd(91, L, d), rnd(92, L, d), rnd(93, L, d)
+    O, lse, _ = A.head_forward(q, k, v, 0.45, causal, slope, window)
+    Oc, lsec = A.head_forward_chunked(q, k, v, 0.45, causal, slope, window, chunk=chunk)
+    np.testing.assert_allclose(Oc, O, atol=1e-12)
+    np.testing.assert_allclose(lsec, lse, atol=1e-12)
+    ref = A.head_backward(q, k, v, do, 0.45, causal, slope, window)
+    got = A.head_backward_chunked(q, k, v, do, 0.45, causal, slope, window, chunk=chunk)
+    for name, r, g in zip(("dQ", "dK", "dV", "O", "LSE", "D"), ref, got):
+        np.testing.assert_allclose(g, r, atol=1e-12, err_msg=name)
+
+
+def test_chunked_head_backward_matches_finite_differences():
+    """Independently of the whole-matrix form: fp64 central differences of
+    <dO, O> (O from the chunked forward) agree with the chunked gradients."""
+    L, d, scale, slope = 7, 3, 0.8, 0.3
+    q, k, v, do = rnd(94, L, d), rnd(95, L, d), rnd(96, L, d), rnd(97, L, d)
+    dq, dk, dv, *_ = A.head_backward_chunked(q, k, v, do, scale, True, slope, chunk=3)
+
+    def f(q_, k_, v_):
+        return float((do * A.head_forward_chunked(q_, k_, v_, scale, True, slope, chunk=2)[0]).sum())
+
+    h = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp = x.copy(); xp[idx] += h
+            xm = x.copy(); xm[idx] -= h
+            ap = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+            am = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+            num[idx] = (f(*ap) - f(*am)) / (2 * h)
+        assert np.max(np.abs(num - g)) / np.max(np.abs(g)) <= 1e-6, name
+
+
 # ------------------------------------------------------------ sliding window
 
 @pytest.mark.parametrize("w", [0, 1, 5, 28])

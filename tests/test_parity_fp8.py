@@ -139,3 +139,44 @@ def test_fp8_accuracy_against_exact_attention_with_outliers():
     print("fp8 rmse vs exact: kernel", e_kernel, "quantization alone", e_oracle)
     assert e_kernel <= 1.25 * e_oracle + 2.0 ** -9
     assert e_kernel < 2e-2
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,head", [("c3_long", 21), ("c5_gqa_alibi", 9)])
+def test_fp8_full_size(name, head):
+    """The benchmark's FP8 workloads at their own size: every code and scale
+    of the whole problem bit for bit, then attention on the dequantized
+    values for sampled rows of every head and for one whole query head
+    (every row, by blocks of rows), at the level-2 bounds above."""
+    w = I.workload(name)
+    x = I.make_inputs(w, seed=0, with_do=False)
+    signs = I.hadamard_signs(128, seed=0)
+    O, lse, buf, lay = _run(x, signs)
+    qz = _check_codes(x, signs, buf, lay)
+    del buf
+    qd = F._dequant(qz["q8"], qz["q_scale"], x.cu_seqlens, w.N)
+    kd = F._dequant(qz["k8"], qz["k_scale"], x.cu_seqlens, w.N)
+    vd = F._dequant(qz["v8"], qz["v_scale"], x.cu_seqlens, w.N)
+    sc = x.scale / w.d                          # Q' and K' carry the transform (Q1)
+    rng = np.random.Generator(np.random.PCG64(77))
+    rows = [(int(t), int(h)) for t, h in zip(rng.integers(0, x.T, 48), rng.integers(0, w.Hq, 48))]
+    rows += [(0, 0), (127, 1), (128, 2), (x.T - 1, w.Hq - 1)]
+    O_r, lse_r = A.forward_rows(qd, kd, vd, sc, w.causal, rows, x.cu_seqlens, x.alibi_slopes)
+    O_g = np.array([O[t, h] for t, h in rows])
+    lse_g = np.array([lse[h, t] for t, h in rows])
+    g = head // (w.Hq // w.Hkv)
+    errs_o, errs_l = [O_g - O_r], [lse_g - lse_r]
+    for b in range(w.B):
+        s, e = int(x.cu_seqlens[b]), int(x.cu_seqlens[b + 1])
+        slope = None if x.alibi_slopes is None else float(x.alibi_slopes[head])
+        Oh, lh = A.head_forward_chunked(qd[s:e, head], kd[s:e, g], vd[s:e, g], sc, w.causal, slope)
+        errs_o.append(O[s:e, head] - Oh)
+        errs_l.append(lse[head, s:e] - lh)
+    eo = np.concatenate([e_.reshape(-1) for e_ in errs_o])
+    el = np.concatenate([e_.reshape(-1) for e_ in errs_l])
+    vdeq = np.abs(vd).max()
+    print(name, "fp8 max |dO|", float(np.abs(eo).max()), "rmse", float(np.sqrt(np.mean(eo ** 2))),
+          "max |dLSE|", float(np.abs(el).max()))
+    assert np.abs(el).max() <= 1e-3
+    assert np.abs(eo).max() <= 2.0 ** -3 * (1 + 2.0 ** -3) * vdeq
+    assert np.sqrt(np.mean(eo ** 2)) <= 2.0 ** -7

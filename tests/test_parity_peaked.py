@@ -1,0 +1,134 @@
+"""Parity in the peaked-softmax regime: scores that span tens to hundreds of
+nats, and row maxima that jump by far more than the lazy-rescale threshold
+between key tiles (GPU).
+
+The online softmax's result does not depend on the running reference max
+("FlashAttention: Faster Attention Without Dropping a Single Interaction",
+Key design 2: the (m, l, O) state merges exactly for any reference), but the
+kernels only reach the paths that move the reference on such inputs:
+
+* the forward's raise of the reference when a tile's max exceeds it by more
+  than tau = 8 (log2 units), with the O rows rescaled in TMEM;
+* the forward's speculative pass whose sum overflows 2^tau;
+* p up to 2^tau stored to bf16 for the PV product;
+* the backward's exp2 of S - LSE when both are hundreds of nats.
+
+Inputs (seeded; ``inputs.add_score_structure`` and ``qk_gain``):
+  ``late_dominant``  keys at offsets 165, 389 and 730 score 1, 2, 3 x s nats
+                     above the rest against every row (s = 30);
+  ``rising``         scores drift up by s = 200 nats along the keys, so the
+                     max rises by about 25 nats per 128-key tile (the
+                     kernels visit unbiased rows' tiles in ascending order);
+  ``falling``        the same drift downwards: with ALiBi the forward
+                     visits tiles from the diagonal backwards;
+  ``qk_gain`` 4, 8   q and k x4 (x8): score spread 16 (64) nats;
+  large ALiBi        slopes x 64: the bias falls by 11 to 54 nats per key.
+
+Element-wise against the fp64 oracle at the stated tolerances: O <= 1e-2,
+LSE <= 1e-3 (absolute, O stored as fp32), each gradient <= 2e-2 x that
+gradient's largest |value|.
+"""
+import numpy as np
+import pytest
+
+from oracle import attention_fp64 as A
+from exact_io_aware_36_gb300 import inputs as I
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+TOL_O, TOL_LSE, TOL_GRAD = 1e-2, 1e-3, 2e-2
+
+STRENGTH = {"late_dominant": 30.0, "rising": 200.0, "falling": 200.0}
+
+
+def make(kind, *, causal, d, alibi=False, B=1, Hq=4, Hkv=2, N=1024, seqlens=None, gain=1.0,
+         slope_mult=1.0, window=None, seed=0):
+    w = I.small_case("bf16", causal=causal, B=B, Hq=Hq, Hkv=Hkv, N=N, d=d, alibi=alibi,
+                     seqlens=seqlens, qk_gain=gain, window=window)
+    x = I.make_inputs(w, seed=seed)
+    if kind is not None:
+        I.add_score_structure(x, kind, STRENGTH[kind], seed=seed + 100)
+    if alibi and slope_mult != 1.0:
+        x.alibi_slopes = (x.alibi_slopes * np.float32(slope_mult)).astype(np.float32)
+    return x
+
+
+def check_forward(x, O, lse):
+    w = x.workload
+    O_r, lse_r = A.attention_forward(x.q, x.k, x.v, x.scale, w.causal, x.cu_seqlens,
+                                     x.alibi_slopes, window=w.window)
+    eo, el = np.abs(O - O_r).max(), np.abs(lse - lse_r).max()
+    print("fwd", w.d, w.causal, w.alibi, {"O": float(eo), "LSE": float(el)},
+          "LSE spread", float(np.nanmax(lse_r) - np.nanmin(lse_r)))
+    assert eo <= TOL_O, eo
+    assert el <= TOL_LSE, el
+
+
+def check_backward(x, O, lse, dq, dk, dv):
+    w = x.workload
+    dq_r, dk_r, dv_r, O_r, lse_r, _ = A.attention_backward(
+        x.q, x.k, x.v, x.do, x.scale, w.causal, x.cu_seqlens, x.alibi_slopes, window=w.window)
+    errs = {"O": np.abs(O - O_r).max(), "LSE": np.abs(lse - lse_r).max()}
+    for name, g, r in (("dQ", dq, dq_r), ("dK", dk, dk_r), ("dV", dv, dv_r)):
+        errs[name] = np.abs(g - r).max() / np.abs(r).max()
+    print("bwd", w.d, w.causal, w.alibi, {k_: float(v_) for k_, v_ in errs.items()})
+    assert errs["O"] <= TOL_O and errs["LSE"] <= TOL_LSE, errs
+    assert errs["dQ"] <= TOL_GRAD and errs["dK"] <= TOL_GRAD and errs["dV"] <= TOL_GRAD, errs
+
+
+FWD_CASES = [
+    # kind, causal, d, alibi, gain, slope_mult
+    ("late_dominant", True, 128, False, 1.0, 1.0),
+    ("late_dominant", False, 64, False, 1.0, 1.0),
+    ("late_dominant", True, 64, True, 1.0, 1.0),
+    ("rising", True, 128, False, 1.0, 1.0),
+    ("rising", False, 128, False, 1.0, 1.0),
+    ("rising", True, 64, False, 1.0, 1.0),
+    ("falling", True, 128, True, 1.0, 1.0),
+    ("falling", False, 64, True, 1.0, 1.0),
+    (None, True, 128, False, 4.0, 1.0),
+    (None, False, 64, False, 8.0, 1.0),
+    (None, True, 128, True, 8.0, 1.0),
+    (None, True, 128, True, 1.0, 64.0),
+    (None, False, 64, True, 1.0, 64.0),
+]
+
+
+@pytest.mark.parametrize("kind,causal,d,alibi,gain,slope_mult", FWD_CASES)
+def test_forward_peaked(kind, causal, d, alibi, gain, slope_mult):
+    x = make(kind, causal=causal, d=d, alibi=alibi, gain=gain, slope_mult=slope_mult,
+             N=1100 if d == 64 else 1024)
+    O, lse = G.forward(x)
+    check_forward(x, O, lse)
+
+
+BWD_CASES = [
+    # kind, causal, d, alibi, gain, slope_mult
+    ("late_dominant", True, 128, False, 1.0, 1.0),
+    ("late_dominant", False, 64, True, 1.0, 1.0),
+    ("rising", True, 128, False, 1.0, 1.0),
+    ("rising", True, 64, False, 1.0, 1.0),
+    ("falling", True, 128, True, 1.0, 1.0),
+    (None, True, 128, False, 4.0, 1.0),
+    (None, False, 64, False, 4.0, 1.0),
+    (None, True, 128, True, 4.0, 1.0),
+    (None, True, 64, True, 1.0, 64.0),
+]
+
+
+@pytest.mark.parametrize("deterministic", [False, True])
+@pytest.mark.parametrize("kind,causal,d,alibi,gain,slope_mult", BWD_CASES)
+def test_backward_peaked(kind, causal, d, alibi, gain, slope_mult, deterministic):
+    x = make(kind, causal=causal, d=d, alibi=alibi, gain=gain, slope_mult=slope_mult, N=1024)
+    O, lse, dq, dk, dv = G.backward(x, deterministic=deterministic)
+    check_backward(x, O, lse, dq, dk, dv)
+
+
+def test_peaked_packed_and_window():
+    """The same regimes on a packed batch (sequence starts that are not tile
+    aligned) and on a causal band, forward and backward."""
+    x = make("late_dominant", causal=True, d=128, seqlens=(800, 37, 1200, 129), seed=5)
+    check_backward(x, *G.backward(x))
+    x = make("rising", causal=True, d=64, N=1500, window=300, seed=6)
+    check_backward(x, *G.backward(x))
