@@ -8,6 +8,7 @@
 
 #include <mutex>
 
+#include "fa_host_util.h"
 #include "fa_internal.h"
 
 namespace {
@@ -422,6 +423,11 @@ fa_status fa_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {
   unsigned int* status = status_ptr();
   if (!status) return FA_ERR_CUDA;
   return fa::launch_selftest_wait(status, limit_ns, stream) == 0 ? FA_OK : FA_ERR_CUDA;
+}
+
+void fa_host_cache_stats(unsigned long long* tmaps_encoded, unsigned long long* tmaps_reused,
+                         unsigned long long* smem_attrs_set) {
+  fa::host_cache_stats(tmaps_encoded, tmaps_reused, smem_attrs_set);
 }
 
 fa_status fa_check_device_error(void* stream) {

@@ -759,8 +759,7 @@ template <int D, bool CAUSAL, bool ALIBI, bool BAND, bool DQ>
 int launch_dkdv(const AttnParams& p, cudaStream_t stream) {
   using C = BwdCfg<D>;
   auto kern = bwd_dkdv_kernel<D, CAUSAL, ALIBI, BAND, DQ>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-  if (e != cudaSuccess) return (int)e;
+  if (const int ea = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES)) return ea;
   CUtensorMap tq, tk, tv, tdo;
   int r = make_tmap_bf16_3d(&tq, p.q, D, p.Hq, p.T, 64);
   if (!r) r = make_tmap_bf16_3d(&tdo, p.dO, D, p.Hq, p.T, 64);
@@ -771,10 +770,8 @@ int launch_dkdv(const AttnParams& p, cudaStream_t stream) {
   // the workspace counter (zeroed by the preprocess and by the previous
   // launch's last CTA).
   const long long nwork = (long long)((p.N + 127) / 128) * p.Hkv * p.B;
-  int dev = 0, nsm = 0;
-  e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return (int)e;
+  int nsm = 0;
+  if (const int es = sm_count(&nsm)) return es;
   dim3 grid((unsigned)std::min<long long>(nwork, nsm));
   kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, p);
   return (int)cudaGetLastError();

@@ -713,9 +713,7 @@ decode_split_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
 }
 
 int launch(const DecodeParams& p, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(decode_split_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       SMEM_BYTES);
-  if (e != cudaSuccess) return (int)e;
+  if (const int ea = set_max_dynamic_smem(reinterpret_cast<const void*>(decode_split_tc_kernel), SMEM_BYTES)) return ea;
   CUtensorMap tq, tk, tv;
   const long long rows = (long long)p.B * p.S_max;
   int r = make_tmap_bf16_3d_box(&tq, p.q, 128, p.Hq, (long long)p.B * p.q_len, p.group, p.q_len);
@@ -785,8 +783,7 @@ template <int D, int RM>
 int launch_split(const DecodeParams& p, cudaStream_t stream) {
   using C = DecCfg<D, RM>;
   auto kern = decode_split_kernel<D, RM>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-  if (e != cudaSuccess) return (int)e;
+  if (const int ea = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES)) return ea;
   CUtensorMap tk, tv;
   const long long rows = (long long)p.B * p.S_max;
   int r = make_tmap_bf16_3d(&tk, p.k, D, p.Hkv, rows, kTileKeys);

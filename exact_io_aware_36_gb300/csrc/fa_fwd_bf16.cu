@@ -510,9 +510,7 @@ template <int D, bool CAUSAL, bool ALIBI, bool BAND>
 int launch_impl(const AttnParams& p, cudaStream_t stream) {
   using C = FwdCfg<D>;
   auto kern = fwd_bf16_kernel<D, CAUSAL, ALIBI, BAND>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM_BYTES);
-  if (e != cudaSuccess) return (int)e;
+  if (const int ea = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES)) return ea;
   CUtensorMap tq, tk, tv, to;
   int r = make_tmap_bf16_3d(&tq, p.q, D, p.Hq, p.T, 128);
   if (!r) r = make_tmap_bf16_3d(&tk, p.k, D, p.Hkv, p.T, 128);

@@ -558,8 +558,7 @@ fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 template <bool CAUSAL, bool ALIBI, bool BAND>
 int launch_impl(const AttnParams& p, cudaStream_t stream) {
   auto kern = fwd_fp8_kernel<CAUSAL, ALIBI, BAND>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
-  if (e != cudaSuccess) return (int)e;
+  if (const int ea = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), Cfg::SMEM_BYTES)) return ea;
   CUtensorMap tq, tk, tv;
   int r = make_tmap_u8_3d(&tq, p.q, kD, p.Hq, p.T, kD, (long long)kD * p.Hq, 128, 1, 128);
   if (!r) r = make_tmap_u8_3d(&tk, p.k, kD, p.Hkv, p.T, kD, (long long)kD * p.Hkv, 128, 1, 128);

@@ -27,7 +27,7 @@ STATUS = {
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_stage", "fa_bwd_workspace_size", "fa_check_device_error",
            "fa_status_string", "fa_version", "fa_bwd_static_scratch", "fa_selftest_wait_timeout",
            "fa_decode", "fa_decode_workspace_size", "fa_fp8_layout_get", "fa_fp8_quantize",
-           "fa_fwd_fp8")
+           "fa_fwd_fp8", "fa_host_cache_stats")
 FA_BWD_PREPROCESS, FA_BWD_DKDV, FA_BWD_DQ_CONVERT = 0, 1, 2
 
 
@@ -178,6 +178,18 @@ def fa_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
     fn.argtypes = [ctypes.c_ulonglong, ctypes.c_void_p]
     fn.restype = ctypes.c_int
     return fn(limit_ns, stream)
+
+
+def fa_host_cache_stats():
+    """(descriptors encoded, descriptors reused, shared-memory limits set)."""
+    lib = load()
+    fn = lib.fa_host_cache_stats
+    u = ctypes.c_ulonglong
+    fn.argtypes = [ctypes.POINTER(u)] * 3
+    fn.restype = None
+    a, b, c = u(), u(), u()
+    fn(ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
+    return a.value, b.value, c.value
 
 
 def fa_check_device_error(stream=None) -> int:

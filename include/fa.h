@@ -37,7 +37,9 @@
  *
  * Pointers: q..dv, lse, cu_seqlens, alibi_slopes and workspace are DEVICE
  * pointers owned by the caller; the library allocates no device memory and
- * keeps no per-call state.  bf16 tensors must start on a 16-byte boundary.
+ * keeps no per-call state: only a per-device status word and a host-side
+ * cache of TMA descriptors per tensor shape and address
+ * (fa_host_cache_stats).  bf16 tensors must start on a 16-byte boundary.
  * `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
  * asynchronous on `stream`; calls are not thread-safe on one stream.
  *
@@ -322,6 +324,22 @@ fa_status fa_check_device_error(void* stream);
  * device, and that the context is usable afterwards.
  */
 fa_status fa_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
+
+/*
+ * Host-side set-up counters since the library was loaded (diagnostic; the
+ * pages have no counterpart).  Each launch needs TMA descriptors for its
+ * tensors and a shared-memory limit for its kernel.  The library keeps the
+ * descriptors in a per-shape cache keyed on (base address, sizes, strides,
+ * box, element type): a call whose tensors match an earlier call's reuses
+ * its descriptors instead of encoding them again, so repeated calls on the
+ * same buffers encode nothing.  The shared-memory limit is set once per
+ * (device, kernel).  Any pointer may be NULL.
+ *   tmaps_encoded   descriptors encoded
+ *   tmaps_reused    descriptors served from the cache
+ *   smem_attrs_set  kernel shared-memory limits set
+ */
+void fa_host_cache_stats(unsigned long long* tmaps_encoded, unsigned long long* tmaps_reused,
+                         unsigned long long* smem_attrs_set);
 
 /* Static description of a status code (never NULL); part of this library's
  * error reporting, with no counterpart on the pages. */
