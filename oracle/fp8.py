@@ -33,7 +33,8 @@ Q2  Blocks are 128 consecutive rows of one head within one sequence (the
 Q3  e4m3 is the OCP E4M3 format without infinities (bias 7, 3 mantissa bits,
     largest finite 448, smallest subnormal 2^-9); rounding is to nearest,
     ties to even, and values beyond 448 saturate to 448 (the kernel's
-    cvt.rn.satfinite).
+    cvt.rn.satfinite).  As in any IEEE-style rounding the sign is kept: a
+    negative value that rounds to zero, and -0 itself, give -0 (code 0x80).
 Q4  V is quantized per block the same way but not transformed (the pages
     apply M to Q and K only).
 Q5  The attention on the quantized values is the exact operator of the FA1
@@ -65,7 +66,7 @@ def e4m3_round(x):
     q = np.exp2(e - 3.0)              # quantum: 2^(e - 3) for normals, 2^-9 below 2^-6
     r = np.rint(a / q) * q            # np.rint: round half to even (a / q is exact)
     r = np.minimum(r, E4M3_MAX)
-    return (np.sign(x) * r).astype(np.float32)
+    return np.copysign(r, x).astype(np.float32)   # the sign survives, zeros too (Q3)
 
 
 def e4m3_bits(x):

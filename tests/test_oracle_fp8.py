@@ -34,6 +34,19 @@ def test_e4m3_round_matches_torch_in_range():
                                   torch.tensor(ours).to(torch.float8_e4m3fn).view(torch.uint8).numpy())
 
 
+def test_e4m3_keeps_the_sign_of_zero():
+    """-0 and negative values that round to zero give -0 (0x80), as the
+    round-to-nearest conversion of PyTorch's float8_e4m3fn does; +0 and
+    positive ones give +0."""
+    torch = pytest.importorskip("torch")
+    x = np.array([-0.0, 0.0, -1e-5, 1e-5, -2.0 ** -10, 2.0 ** -10, -2.0 ** -11, -1e-30],
+                 dtype=np.float32)
+    ours = F.e4m3_bits(F.e4m3_round(x))
+    ref = torch.tensor(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(ours, ref)
+    np.testing.assert_array_equal(ours, [0x80, 0, 0x80, 0, 0x80, 0, 0x80, 0x80])
+
+
 def test_e4m3_saturates_and_ties_to_even():
     x = np.array([449, 464, 470, 1e6, -1e6, 2 ** -10, 3 * 2 ** -10, 1.0625, 1.1875, 17.0],
                  dtype=np.float32)
