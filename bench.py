@@ -584,7 +584,8 @@ def run_fp8(args, world, rank, local):
                      "ptrs": (P(q2), P(k2), P(v2), P(o2), P(lse2))})
         host = lambda n: torch.from_numpy(x.bits[n].view("int16")).view(torch.bfloat16)
         e2e = run_e2e(args, {"total": fl}, world, dev, stream, step,
-                      [host("q"), host("k"), host("v")], sets, "fa_fp8_quantize + fa_fwd_fp8")
+                      [host("q"), host("k"), host("v")], sets, "fa_fp8_quantize + fa_fwd_fp8",
+                      kernel_ms=ms_step)
     line = {
         "metric": FP8_METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
@@ -642,7 +643,7 @@ def run_ours(args, world, rank, local):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     cu = torch.from_numpy(x.cu_seqlens).to(dev) if w.varlen else None
     slopes = torch.from_numpy(x.alibi_slopes).to(dev) if w.alibi else None
-    ws_bytes = fa.fa_bwd_workspace_size(w.B, w.Hq, w.N, w.d, T)
+    ws_bytes = fa.fa_bwd_workspace_size_gqa(w.B, w.Hq, w.Hkv, w.N, w.d, T)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
@@ -651,7 +652,11 @@ def run_ours(args, world, rank, local):
               P(slopes))
     ptrs = (P(q), P(k), P(v), P(o), P(do), P(lse), P(dq), P(dk), P(dv))
     det = 1 if args.deterministic else 0
-    names = ["fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq" if det else "bwd_dq_convert"]
+    # grouped-query problems split their dK/dV items when the workspace has
+    # room for the per-part sums; stage 2 then also adds the parts up
+    kv_split = w.backward and ws_bytes > fa.fa_bwd_workspace_size(w.B, w.Hq, w.N, w.d, T)
+    names = ["fwd", "bwd_preprocess", "bwd_dkdv",
+             ("bwd_dq" if det else "bwd_dq_convert") + ("+dkdv_convert" if kv_split else "")]
 
     def step(evs=None, ptrs=ptrs):
         if evs is not None:
@@ -771,7 +776,7 @@ def run_ours(args, world, rank, local):
                          "ptrs": (P(bq), P(bk), P(bv), P(bo), P(bdo), P(blse), P(bdq), P(bdk),
                                   P(bdv))})
         e2e = run_e2e(args, fl, world, dev, stream, step, [host(n) for n in in_names], sets,
-                      "fa_fwd + fa_bwd_stage x3" if w.backward else "fa_fwd")
+                      "fa_fwd + fa_bwd_stage x3" if w.backward else "fa_fwd", kernel_ms=ms_step)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -786,7 +791,7 @@ def run_ours(args, world, rank, local):
         "data": "synthetic (seeded PCG64, seed 0; no dataset)",
         "config": {"workload": w.name, "desc": w.note, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
                    "N": w.N, "d": w.d, "causal": w.causal, "window": w.window,
-                   "deterministic_bwd": bool(det),
+                   "deterministic_bwd": bool(det), "dkdv_split": 2 if kv_split else 1,
                    "alibi": w.alibi, "varlen": w.varlen,
                    "total_tokens": T, "o_dtype": "fp32", "flops_per_step": fl["total"],
                    "pct_of_peak": None if fp32 else round(100.0 * value / world / peak, 2),
@@ -798,7 +803,7 @@ def run_ours(args, world, rank, local):
         "per_kernel": per_kernel,
         "roofline": roof,
         "secondary_roofs": None if fp32 else secondary_roofs(w, T, fl, kern_ms, dev, hbm, bool(det)),
-        "gpu_launches": args.steps * (4 if w.backward else 1),
+        "gpu_launches": args.steps * ((5 if kv_split else 4) if w.backward else 1),
         "clocks": clocks,
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -807,7 +812,63 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, fl, world, dev, stream, step, host_ins, sets, calls):
+def gpu_numa_cpus(dev):
+    """(NUMA node of the GPU, the CPUs of that node this process may use), from
+    sysfs; (None, None) when either is unknown."""
+    import torch
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        bus = f"{pr.pci_domain_id:04x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+        node = int(open(f"/sys/bus/pci/devices/{bus}/numa_node").read().strip())
+        if node < 0:
+            return None, None
+        cpus = set()
+        for part in open(f"/sys/devices/system/node/node{node}/cpulist").read().strip().split(","):
+            lo, _, hi = part.partition("-")
+            cpus.update(range(int(lo), int(hi or lo) + 1))
+        cpus &= os.sched_getaffinity(0)
+        return node, sorted(cpus) if cpus else None
+    except (OSError, ValueError, AttributeError):
+        return None, None
+
+
+def copy_rates(dev, hins, dins, houts, douts, s_in, s_out, reps=3):
+    """GB/s of one step's input copies alone (host to device), output copies
+    alone (device to host), and both at once on their two streams."""
+    import torch
+    bi = sum(h.numel() * h.element_size() for h in hins)
+    bo = sum(h.numel() * h.element_size() for h in houts)
+
+    def timed(do_in, do_out):
+        best = None
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            a = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            a[0].record(s_in)
+            a[2].record(s_out)
+            if do_in:
+                with torch.cuda.stream(s_in):
+                    for d, h in zip(dins, hins):
+                        d.copy_(h, non_blocking=True)
+            if do_out:
+                with torch.cuda.stream(s_out):
+                    for h, d in zip(houts, douts):
+                        h.copy_(d, non_blocking=True)
+            a[1].record(s_in)
+            a[3].record(s_out)
+            torch.cuda.synchronize(dev)
+            ms = max(a[0].elapsed_time(a[1]) if do_in else 0.0,
+                     a[2].elapsed_time(a[3]) if do_out else 0.0)
+            best = ms if best is None else min(best, ms)
+        return best
+
+    t_in, t_out, t_both = timed(True, False), timed(False, True), timed(True, True)
+    return {"h2d_gbs": round(bi / (t_in * 1e-3) / 1e9, 1), "d2h_gbs": round(bo / (t_out * 1e-3) / 1e9, 1),
+            "both_gbs": round((bi + bo) / (t_both * 1e-3) / 1e9, 1),
+            "h2d_ms": round(t_in, 3), "d2h_ms": round(t_out, 3), "both_ms": round(t_both, 3)}
+
+
+def run_e2e(args, fl, world, dev, stream, step, host_ins, sets, calls, kernel_ms=None):
     """Same metric through the C ABI with host buffers: every step copies its
     inputs from pinned host memory and its outputs back to pinned host
     memory, and all of those copies are inside the timed region.  The steps
@@ -815,13 +876,31 @@ def run_e2e(args, fl, world, dev, stream, step, host_ins, sets, calls):
     compute stream, buffer set i % 2) overlap the copy of step i+1's inputs
     (copy-in stream) and of step i-1's outputs (copy-out stream).  A set is
     refilled only after the kernels that read it are done, and overwritten
-    only after its outputs have been copied out."""
+    only after its outputs have been copied out.
+
+    The pinned buffers are allocated with the process bound to the CPUs of
+    the GPU's NUMA node (where the system says which that is), so that their
+    pages are local to the GPU's host link.  The copy rates of one step's
+    inputs and outputs, alone and together, are measured beside the timed
+    steps; with the kernels' own time they say how much of the copying the
+    pipeline hid."""
     import torch
-    hins = [h.pin_memory() for h in host_ins]
-    houts = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in sets[0]["outs"]]
+    node, cpus = gpu_numa_cpus(dev)
+    old_aff = os.sched_getaffinity(0)
+    if cpus:
+        os.sched_setaffinity(0, cpus)
+    try:
+        hins = [h.pin_memory() for h in host_ins]
+        houts = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in sets[0]["outs"]]
+        for h in houts:
+            h.zero_()                                  # touch the pages on this node
+    finally:
+        if cpus:
+            os.sched_setaffinity(0, old_aff)
     h2d = sum(h.numel() * h.element_size() for h in hins)
     d2h = sum(h.numel() * h.element_size() for h in houts)
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    rates = copy_rates(dev, hins, sets[1]["ins"], houts, sets[1]["outs"], s_in, s_out)
     comp_done, out_done = [None, None], [None, None]
 
     def run(n):
@@ -852,7 +931,7 @@ def run_e2e(args, fl, world, dev, stream, step, host_ins, sets, calls):
 
     run(2)
     torch.cuda.synchronize(dev)
-    n = max(3, args.steps // 3)
+    n = max(3, args.steps)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     s_in.wait_event(e0)
@@ -862,11 +941,22 @@ def run_e2e(args, fl, world, dev, stream, step, host_ins, sets, calls):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     ms = e0.elapsed_time(e1) / n
-    return {"value": round(world * fl["total"] / (ms * 1e-3) / 1e12, 2 if fl["total"] > 1e9 else 5),
-            "unit": UNIT, "ms_per_step": round(ms, 3), "steps": n, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h,
-            "path": calls + " through the C ABI; pinned host buffers; copies of step i+1's inputs "
-                    "and step i-1's outputs overlap step i's kernels (three streams, two buffer sets)"}
+    out = {"value": round(world * fl["total"] / (ms * 1e-3) / 1e9 / 1e3, 2 if fl["total"] > 1e9 else 5),
+           "unit": UNIT, "ms_per_step": round(ms, 3), "steps": n, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "copy_rates": rates,
+           "pinned_numa_node": node, "pinned_bound_cpus": len(cpus) if cpus else None,
+           "path": calls + " through the C ABI; pinned host buffers; copies of step i+1's inputs "
+                   "and step i-1's outputs overlap step i's kernels (three streams, two buffer sets)"}
+    if kernel_ms is not None:
+        # Without overlap a step would take kernels + both copies; fully
+        # overlapped, the larger of the kernels and the concurrent copies.
+        serial = kernel_ms + rates["h2d_ms"] + rates["d2h_ms"]
+        hidden = max(kernel_ms, rates["both_ms"])
+        out["kernel_ms_per_step"] = round(kernel_ms, 3)
+        out["serial_ms_per_step"] = round(serial, 3)
+        out["overlapped_bound_ms"] = round(hidden, 3)
+        out["copy_hidden_frac"] = round(min(1.0, max(0.0, (serial - ms) / max(serial - hidden, 1e-9))), 3)
+    return out
 
 
 # ---------------------------------------------------------------- CPU oracle

@@ -6,6 +6,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "fa_host_util.h"
@@ -144,6 +145,46 @@ size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, long long total_tokens
   return round256((size_t)Hq * T * sizeof(float)) + round256((size_t)Hq * T * d * sizeof(float)) + 256;
 }
 
+// dK / dV work items per (key tile, kv head, sequence) for a group of
+// `group` query heads: 2 (halves of the group) when the group splits evenly.
+static int gqa_split(int Hq, int Hkv) {
+  const int group = Hkv > 0 ? Hq / Hkv : 0;
+  return (group >= 2 && group % 2 == 0) ? 2 : 1;
+}
+
+// Whether the dK/dV work items of a dense batch are too few and too large to
+// spread evenly over the SMs: the largest item (key tile 0: every query tile
+// of every head of the group) against a quarter of the steps per SM.  Each
+// SM takes its next item when it finishes one, largest first; with items
+// this large the last ones leave SMs idle for a good part of an item.
+// Packed batches (sizes unknown on the host) are never split.
+static bool dkdv_items_uneven(int B, int group, int Hkv, int N, int causal, int window) {
+  int nsm = 0;
+  if (fa::sm_count(&nsm) != 0 || nsm <= 0) return false;
+  const long long nkt = (N + 127) / 128, nqt_all = (N + 63) / 64;
+  long long total = 0, largest = 0;
+  for (long long kt = 0; kt < nkt; ++kt) {
+    const long long qt0 = causal ? 2 * kt : 0;
+    long long qt_end = nqt_all;
+    if (causal && window != fa::kNoWindow)
+      qt_end = std::min(nqt_all, (kt * 128 + 127 + window) / 64 + 1);
+    const long long steps = (long long)group * std::max(0ll, qt_end - qt0);
+    total += steps;
+    largest = std::max(largest, steps);
+  }
+  total *= (long long)B * Hkv;
+  return largest * 4 > total / nsm;
+}
+
+size_t fa_bwd_workspace_size_gqa(int B, int Hq, int Hkv, int N, int d, long long total_tokens) {
+  const size_t base = fa_bwd_workspace_size(B, Hq, N, d, total_tokens);
+  if (base == 0 || Hkv <= 0 || Hq % Hkv != 0) return 0;
+  const int split = gqa_split(Hq, Hkv);
+  if (split == 1) return base;
+  const long long T = total_tokens > 0 ? total_tokens : (long long)B * N;
+  return base + round256((size_t)split * 2 * T * Hkv * d * sizeof(float));
+}
+
 }  // extern "C"
 
 namespace fa {
@@ -206,6 +247,15 @@ static fa_status bwd_impl(int stage, const void* q, const void* k, const void* v
                                       round256((size_t)Hq * T * sizeof(float)));
   p.work_ctr = reinterpret_cast<int*>(static_cast<char*>(workspace) + round256((size_t)Hq * T * sizeof(float)) +
                                       round256((size_t)Hq * T * d * sizeof(float)));
+  // A workspace of fa_bwd_workspace_size_gqa bytes also holds per-part dK /
+  // dV sums, which lets the dK/dV kernel split each GQA group's work.
+  p.kv_split = 1;
+  if (!cu_seqlens && gqa_split(Hq, Hkv) > 1 &&
+      dkdv_items_uneven(B, Hq / Hkv, Hkv, N, causal, p.window) &&
+      workspace_bytes >= fa_bwd_workspace_size_gqa(B, Hq, Hkv, N, d, cu_seqlens ? T : 0)) {
+    p.kv_split = gqa_split(Hq, Hkv);
+    p.dkv_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + need);
+  }
   p.status = status_ptr();
   if (!p.status) return FA_ERR_CUDA;
   const int e = fa::launch_bwd_bf16(p, stream, stage);

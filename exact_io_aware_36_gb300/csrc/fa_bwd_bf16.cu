@@ -195,6 +195,35 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const AttnParams p)
   reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dq) + (t * p.Hq + h) * D + c8 * 8)[0] = out;
 }
 
+// ------------------------------------------------------- dK/dV parts convert
+// Split dK/dV items (kv_split > 1): dK = scale * sum of the parts, dV = sum of
+// the parts, in part order (deterministic), -> bf16 [T, Hkv, d].
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dkdv_convert_kernel(const AttnParams p) {
+  const long long e = (long long)blockIdx.x * 256 + threadIdx.x;   // one per 8 outputs
+  const long long per = p.T * p.Hkv * (D / 8);
+  if (e >= 2 * per) return;
+  const int which = e >= per;                    // 0: dK, 1: dV
+  const long long off = (e - which * per) * 8;   // element offset in [T, Hkv, d]
+  const long long slot = p.T * p.Hkv * D;
+  float a[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a[i] = 0.f;
+  for (int r = 0; r < p.kv_split; ++r) {
+    const float4* src = reinterpret_cast<const float4*>(p.dkv_part + (long long)(2 * r + which) * slot + off);
+    const float4 x = src[0], y = src[1];
+    a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
+    a[4] += y.x; a[5] += y.y; a[6] += y.z; a[7] += y.w;
+  }
+  const float f = which ? 1.f : p.scale;
+  uint4 out;
+  out.x = pack_bf16x2(a[0] * f, a[1] * f);
+  out.y = pack_bf16x2(a[2] * f, a[3] * f);
+  out.z = pack_bf16x2(a[4] * f, a[5] * f);
+  out.w = pack_bf16x2(a[6] * f, a[7] * f);
+  reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(which ? p.dv : p.dk) + off)[0] = out;
+}
+
 // ---------------------------------------------------------------------- dkdv
 // Work item w (a key tile of 128 rows of one kv head of one sequence) in
 // launch order.  Dense batches: key tile slowest, so with a causal mask the
@@ -208,11 +237,17 @@ struct DkdvItem {
   long long seq0;        // first token of the sequence
   int L;                 // sequence length
   int qt0, nqt, n_iter;  // first query tile, query tiles per head, steps
+  int h0, part;          // first query head of the item; its part of the group
 };
 
 template <bool CAUSAL, bool BAND>
 __device__ __forceinline__ bool dkdv_item(const AttnParams& p, int w, DkdvItem& it) {
   const int nkt = (p.N + 127) / 128;
+  // With kv_split > 1 the parts of one (key tile, kv head, sequence) are
+  // adjacent items: they run at the same time on different SMs and share
+  // its K / V through L2.  Part r takes query heads g*group + r*group/split ...
+  it.part = w % p.kv_split;
+  w /= p.kv_split;
   if (p.cu_seqlens) {
     const int gb = w / nkt;
     it.g = gb % p.Hkv;
@@ -232,7 +267,9 @@ __device__ __forceinline__ bool dkdv_item(const AttnParams& p, int w, DkdvItem& 
   it.qt0 = CAUSAL ? it.n0 / 64 : 0;
   const int qt_end = BAND ? min(nqt_all, (it.n0 + 127 + p.window) / 64 + 1) : nqt_all;
   it.nqt = qt_end - it.qt0;
-  it.n_iter = p.group * it.nqt;
+  const int heads = p.group / p.kv_split;
+  it.h0 = it.g * p.group + it.part * heads;
+  it.n_iter = heads * it.nqt;
   return true;
 }
 
@@ -265,7 +302,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int nwork = ((p.N + 127) / 128) * p.Hkv * p.B;
+  const int nwork = ((p.N + 127) / 128) * p.Hkv * p.B * p.kv_split;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
@@ -355,7 +392,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const int s = G + i;
         const int st = s % kQStages;
         if (!wait_warp(&bars->q_empty[st], ((s / kQStages) & 1) ^ 1, wc)) return false;
-        const int h = it.g * p.group + i / it.nqt;
+        const int h = it.h0 + i / it.nqt;
         const int q0 = (it.qt0 + i % it.nqt) * 64;
         if (lane == 0) {
           mbar_arrive_expect_tx(&bars->q_full[st], 2 * C::Q_TILE);
@@ -655,19 +692,30 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {        // 0: dV, 1: dK (times the scale)
         const float f = which ? sc : 1.f;
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(which ? p.dk : p.dv) +
-                             ((itm.seq0 + key) * p.Hkv + itm.g) * D;
+        const long long row = (itm.seq0 + key) * p.Hkv + itm.g;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(which ? p.dk : p.dv) + row * D;
+        // split items: this part's fp32 sums go to its own slot, summed in a
+        // fixed order by the convert kernel (dK's scale is applied there)
+        float* part_dst = p.kv_split > 1
+            ? p.dkv_part + ((long long)(itm.part * 2 + (1 - which)) * p.T * p.Hkv + row) * D : nullptr;
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t r[32];
           tmem_ld32(lane_base + (which ? C::DK_COL : C::DV_COL) + c0, r);
           tmem_wait_ld();
           reg_fence32(r);
-          uint32_t pkd[16];
+          if (!key_ok) continue;
+          if (part_dst) {
+            float4* d4 = reinterpret_cast<float4*>(part_dst + c0);
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pkd[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * f, __uint_as_float(r[2 * e + 1]) * f);
-          if (key_ok) {
+            for (int v4 = 0; v4 < 8; ++v4)
+              d4[v4] = make_float4(__uint_as_float(r[4 * v4]), __uint_as_float(r[4 * v4 + 1]),
+                                   __uint_as_float(r[4 * v4 + 2]), __uint_as_float(r[4 * v4 + 3]));
+          } else {
+            uint32_t pkd[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              pkd[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * f, __uint_as_float(r[2 * e + 1]) * f);
             uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4) d4[v4] = make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
@@ -695,7 +743,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       for (int i = 0; DQ && i < itm.n_iter; ++i) {
         const int s = G + i;
         const int buf = s & 1;
-        const int h = itm.g * p.group + i / itm.nqt;
+        const int h = itm.h0 + i / itm.nqt;
         const int q0 = (itm.qt0 + i % itm.nqt) * 64;
         const int nvalid = min(64, itm.L - q0);
         if (!(ok = wait_warp(&bars->dq_full, s & 1, wc))) break;
@@ -769,7 +817,7 @@ int launch_dkdv(const AttnParams& p, cudaStream_t stream) {
   // Persistent: one CTA per SM (at most one per item), items handed out by
   // the workspace counter (zeroed by the preprocess and by the previous
   // launch's last CTA).
-  const long long nwork = (long long)((p.N + 127) / 128) * p.Hkv * p.B;
+  const long long nwork = (long long)((p.N + 127) / 128) * p.Hkv * p.B * p.kv_split;
   int nsm = 0;
   if (const int es = sm_count(&nsm)) return es;
   dim3 grid((unsigned)std::min<long long>(nwork, nsm));
@@ -802,6 +850,12 @@ int launch_stages(const AttnParams& p, cudaStream_t stream, int stage) {
     if (r) return r;
   }
   if (stage < 0 || stage == 2) {
+    if (p.kv_split > 1) {
+      const long long n8 = 2 * p.T * p.Hkv * (D / 8);
+      bwd_dkdv_convert_kernel<D><<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(p);
+      const cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return (int)e;
+    }
     if (p.deterministic) return launch_bwd_dq_bf16(p, stream);
     const long long n8 = rows * (D / 8);
     bwd_dq_convert_kernel<D><<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(p);

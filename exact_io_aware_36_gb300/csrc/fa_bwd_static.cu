@@ -73,7 +73,9 @@ extern "C" fa_status fa_bwd_static_scratch(
   // Everything the kernels read from the scratch is written by the same call
   // first: D by the preprocess kernel, and the dQ accumulator is zeroed
   // there too, so the previous call's contents never leak into this one.
+  // The workspace is declared at the size fa_bwd_workspace_size gives, so the
+  // same schedule runs as for a caller who allocated exactly that much.
   return fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, causal, window,
-                cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype, deterministic, ws,
-                (size_t)FA_BWD_STATIC_SCRATCH_BYTES, stream);
+                cu_seqlens, total_tokens, alibi_slopes, dtype, o_dtype, deterministic, ws, need,
+                stream);
 }

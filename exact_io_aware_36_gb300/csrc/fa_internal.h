@@ -32,6 +32,10 @@ struct AttnParams {
   float* D;          // workspace: D_i = dO_i . O_i, [Hq, T]
   float* dq_acc;     // workspace: fp32 dQ accumulator, [Hq, T, d]
   int* work_ctr;     // workspace: dK/dV work-item counter, finished-CTA count
+  float* dkv_part;   // workspace (kv_split > 1): fp32 dK / dV partial sums,
+                     // [kv_split][2][T, Hkv, d] (part, then 0: dK, 1: dV)
+  int kv_split;      // dK/dV work items per (key tile, kv head, sequence):
+                     // the group's query heads are split into this many parts
   const int32_t* cu_seqlens;   // [B+1] or nullptr
   const float* alibi;          // [Hq] or nullptr
   unsigned int* status;        // per-device status word
@@ -127,7 +131,9 @@ fa_status bwd_check_args(const void* q, const void* k, const void* v, const void
 
 // Launchers (each returns a cudaError_t value as int).
 int launch_fwd_fp32(const AttnParams& p, void* stream);
-int launch_fwd_bf16(const AttnParams& p, void* stream);
+int launch_fwd_bf16(const AttnParams& p, void* stream);             // picks one of:
+int launch_fwd_bf16_block(const AttnParams& p, void* stream);       //   one CTA per query block
+int launch_fwd_bf16_persistent(const AttnParams& p, void* stream);  //   one CTA per SM
 int launch_bwd_bf16(const AttnParams& p, void* stream, int stage);   // stage < 0: all
 int launch_bwd_dq_bf16(const AttnParams& p, void* stream);            // deterministic dQ
 int launch_decode_bf16(const DecodeParams& p, void* stream);          // split + combine

@@ -157,6 +157,27 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const 
   return wait_warp_slow(bar, parity, w.abort_flag, w.status, w.limit_ns);
 }
 
+// wait_warp with the slow path inlined, for kernels whose warpgroups change
+// their register limits (setmaxnreg): ptxas cannot allocate registers around
+// a call there.
+__device__ __forceinline__ bool wait_warp_inl(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    int bad = 0;
+    if ((threadIdx.x & 31) == 0) {
+      if (*w.abort_flag) bad = 1;
+      else if (globaltimer_ns() - t0 > w.limit_ns) {
+        *w.abort_flag = 1;
+        record_status(w.status, FA_ERR_DEVICE_TIMEOUT);
+        bad = 1;
+      }
+    }
+    if (__shfl_sync(0xffffffffu, bad, 0)) return false;
+  }
+}
+
 // Bounded wait that ignores the abort flag, used while unwinding: copies and
 // MMAs already in flight must land before shared memory or TMEM is released.
 __device__ __forceinline__ bool wait_warp_drain(uint64_t* bar, uint32_t parity) {
@@ -188,6 +209,22 @@ __device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t nthreads, bo
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r) : "r"((uint32_t)pred), "r"(id), "r"(nthreads) : "memory");
   return r != 0;
+}
+
+// ------------------------------------------------------- register budgets
+
+// Raise / lower this warpgroup's per-thread register limit (all warps of the
+// warpgroup execute the same instruction).  The raises of a CTA draw on the
+// registers its lowered warpgroups give back, so the sum over warpgroups of
+// (limit x 128 threads) must stay within what the CTA was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void regs_raise() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(N));
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void regs_lower() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(N));
 }
 
 // ------------------------------------------------------------------ fences

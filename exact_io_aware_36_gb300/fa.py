@@ -27,7 +27,7 @@ STATUS = {
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_stage", "fa_bwd_workspace_size", "fa_check_device_error",
            "fa_status_string", "fa_version", "fa_bwd_static_scratch", "fa_selftest_wait_timeout",
            "fa_decode", "fa_decode_workspace_size", "fa_fp8_layout_get", "fa_fp8_quantize",
-           "fa_fwd_fp8", "fa_host_cache_stats")
+           "fa_fwd_fp8", "fa_host_cache_stats", "fa_bwd_workspace_size_gqa")
 FA_BWD_PREPROCESS, FA_BWD_DKDV, FA_BWD_DQ_CONVERT = 0, 1, 2
 
 
@@ -73,6 +73,8 @@ def load(path: Optional[str] = None):
     lib.fa_bwd_stage.restype = i
     lib.fa_bwd_workspace_size.argtypes = [i, i, i, i, ll]
     lib.fa_bwd_workspace_size.restype = sz
+    lib.fa_bwd_workspace_size_gqa.argtypes = [i, i, i, i, i, ll]
+    lib.fa_bwd_workspace_size_gqa.restype = sz
     lib.fa_decode_workspace_size.argtypes = [i, i, i, i, i, i]
     lib.fa_decode_workspace_size.restype = sz
     lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, i, vp, sz, vp]
@@ -169,6 +171,10 @@ def fa_fwd_fp8(fp8_buf, fp8_bytes, o, lse, B, Hq, Hkv, N, d, scale, causal, wind
 
 def fa_bwd_workspace_size(B, Hq, N, d, total_tokens) -> int:
     return load().fa_bwd_workspace_size(B, Hq, N, d, total_tokens)
+
+
+def fa_bwd_workspace_size_gqa(B, Hq, Hkv, N, d, total_tokens) -> int:
+    return load().fa_bwd_workspace_size_gqa(B, Hq, Hkv, N, d, total_tokens)
 
 
 def fa_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
@@ -275,8 +281,9 @@ def attention_backward(q, k, v, o, dO, lse, *, causal: bool, scale: Optional[flo
                        workspace=None, dq=None, dk=None, dv=None, stream=None,
                        check: bool = False):
     """dQ, dK, dV through ``fa_bwd`` (bf16).  ``workspace`` (uint8 device
-    tensor of at least ``fa_bwd_workspace_size`` bytes) is allocated when
-    not given.  ``window`` as in attention_forward; ``deterministic`` selects
+    tensor of at least ``fa_bwd_workspace_size`` bytes; the default is
+    ``fa_bwd_workspace_size_gqa``'s size, which lets grouped-query problems
+    split their dK/dV work) is allocated when not given.  ``window`` as in attention_forward; ``deterministic`` selects
     the backward whose results do not vary from run to run."""
     import torch
     T, B, Hq, Hkv, N, d = _sizes(q, k, cu_seqlens, max_seqlen, batch)
@@ -284,7 +291,7 @@ def attention_backward(q, k, v, o, dO, lse, *, causal: bool, scale: Optional[flo
         raise TypeError("fa_bwd takes bf16 tensors")
     if scale is None:
         scale = d ** -0.5
-    need = fa_bwd_workspace_size(B, Hq, N, d, T)
+    need = fa_bwd_workspace_size_gqa(B, Hq, Hkv, N, d, T)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     dq = torch.empty_like(q) if dq is None else dq

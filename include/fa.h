@@ -118,6 +118,24 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, long long total_tokens);
 
 /*
+ * A larger workspace for grouped-query problems (Hq / Hkv even and >= 2):
+ * fa_bwd_workspace_size plus room for two per-part sums of dK and dV
+ * (float32 [2][2][T, Hkv, d]).  Given at least this many bytes, fa_bwd
+ * splits the dK/dV work of each (key tile, kv head, sequence) between two
+ * blocks, each taking half of the group's query heads; their sums are added
+ * in a fixed order by the last stage, so results stay reproducible.  This
+ * evens out the work per SM when the group's work items are few and large
+ * (e.g. B=2, Hq=32, Hkv=4, N=8192: 512 items of up to 1024 steps on 152
+ * SMs).  fa_bwd splits only dense batches whose largest item exceeds a
+ * quarter of the average work per SM; otherwise, or with a smaller
+ * workspace, the work is not split.  When it is split, FA_BWD_DKDV leaves
+ * the parts in the workspace and FA_BWD_DQ_CONVERT writes dk and dv.
+ * Returns fa_bwd_workspace_size's value when the problem is never split
+ * (Hq / Hkv odd or 1), 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_size_gqa(int B, int Hq, int Hkv, int N, int d, long long total_tokens);
+
+/*
  * Backward: from q, k, v, the forward's o (element type o_dtype) and lse,
  * and dO, writes dq ([T, Hq, d]), dk and dv ([T, Hkv, d]), all bf16.  Same
  * size, mask and window arguments as fa_fwd.  `workspace` (device,
@@ -149,10 +167,13 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
  *   FA_BWD_PREPROCESS  D = rowsum(dO o O) and the dQ accumulator zeroed
  *                      (both in the workspace; deterministic: D only)
  *   FA_BWD_DKDV        dk, dv, and dQ accumulated in the workspace
- *                      (deterministic: dk and dv only)
+ *                      (deterministic: dk and dv only; with split GQA
+ *                      work, see fa_bwd_workspace_size_gqa, the dK / dV
+ *                      parts in the workspace instead of dk and dv)
  *   FA_BWD_DQ_CONVERT  dq = scale * accumulator, as bf16 (deterministic:
  *                      dq computed by its own kernel from q, k, v, dO, lse
- *                      and D, one query tile per block)
+ *                      and D, one query tile per block); with split GQA
+ *                      work also dk and dv from their parts
  * The same checks as fa_bwd run first; an unknown stage is
  * FA_ERR_UNSUPPORTED.
  * FA_BWD_DKDV hands out its work items from a counter in the workspace that

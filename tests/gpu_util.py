@@ -71,9 +71,13 @@ def forward(x: I.Inputs, guard=True, check=True, out_dtype=None):
     return as_f64(o), as_f64(lse)
 
 
-def backward(x: I.Inputs, guard=True, check=True, out_dtype=None, deterministic=False):
+def backward(x: I.Inputs, guard=True, check=True, out_dtype=None, deterministic=False,
+             base_workspace=False):
     """Run fa_fwd then fa_bwd; returns float64 numpy (O, LSE, dQ, dK, dV).
-    O is stored as fp32 unless `out_dtype` says otherwise."""
+    O is stored as fp32 unless `out_dtype` says otherwise.  The workspace is
+    the binding's default (fa_bwd_workspace_size_gqa bytes), or exactly
+    fa_bwd_workspace_size bytes with `base_workspace` (grouped-query dK/dV
+    work then is not split)."""
     t = torch()
     w = x.workload
     q, k, v, do = (to_dev(x, n) for n in ("q", "k", "v", "do"))
@@ -84,8 +88,14 @@ def backward(x: I.Inputs, guard=True, check=True, out_dtype=None, deterministic=
     o, lse = fa.attention_forward(q, k, v, out_dtype=out_dtype or t.float32, **kw)
     bufs = [guarded_empty(q.shape, q.dtype), guarded_empty(k.shape, k.dtype),
             guarded_empty(v.shape, v.dtype)]
+    ws = None
+    if base_workspace:
+        ws = t.empty(max(fa.fa_bwd_workspace_size(w.B if not w.varlen else len(x.cu_seqlens) - 1,
+                                                  w.Hq, w.N, w.d, x.T), 1),
+                     dtype=t.uint8, device="cuda")
     dq, dk, dv = fa.attention_backward(q, k, v, o, do, lse, dq=bufs[0][1], dk=bufs[1][1],
-                                       dv=bufs[2][1], deterministic=deterministic, **kw)
+                                       dv=bufs[2][1], deterministic=deterministic, workspace=ws,
+                                       **kw)
     t.cuda.synchronize()
     if guard:
         for b, _ in bufs:

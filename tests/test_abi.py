@@ -146,3 +146,16 @@ def test_decode_workspace_size(lib):
     assert n == units * 4 * 128 * 4 + ((units * 4 * 3 * 4 + 255) // 256) * 256
     assert fa.fa_decode_workspace_size(1, 3, 2, 64, 1, 64) == 0      # Hq % Hkv != 0
     assert fa.fa_decode_workspace_size(1, 32, 1, 64, 1, 64) == 0     # 32 rows
+
+
+def test_gqa_workspace_size(lib):
+    """The grouped-query workspace adds two per-part sums of dK and dV
+    (float32 [2][2][T, Hkv, d], 256-byte aligned) when Hq / Hkv is even,
+    and equals the base size otherwise."""
+    base = fa.fa_bwd_workspace_size(2, 32, 8192, 128, 0)
+    assert fa.fa_bwd_workspace_size_gqa(2, 32, 4, 8192, 128, 0) == base + 2 * 2 * 16384 * 4 * 128 * 4
+    assert fa.fa_bwd_workspace_size_gqa(2, 32, 32, 8192, 128, 0) == base
+    assert fa.fa_bwd_workspace_size_gqa(1, 6, 2, 100, 64, 0) == fa.fa_bwd_workspace_size(1, 6, 100, 64, 0)
+    assert fa.fa_bwd_workspace_size_gqa(1, 6, 4, 100, 64, 0) == 0        # Hq % Hkv != 0
+    assert fa.fa_bwd_workspace_size_gqa(3, 8, 1, 0, 64, 1000) == \
+        fa.fa_bwd_workspace_size(3, 8, 0, 64, 1000) + ((2 * 2 * 1000 * 1 * 64 * 4 + 255) // 256) * 256

@@ -57,8 +57,8 @@ def test_repeated_calls_encode_nothing(lib):
     e1, r1, a1 = fa.fa_host_cache_stats()
     assert e1 == e0, "a repeated call encoded descriptors again"
     assert a1 == a0, "a repeated call set a shared-memory limit again"
-    # forward: q, k, v, o; dK/dV kernel: q, dO, k, v; three calls
-    assert r1 - r0 >= 3 * 8
+    # forward: q, k, v; dK/dV kernel: q, dO, k, v; three calls
+    assert r1 - r0 >= 3 * 7
     assert fa.fa_check_device_error() == 0
     # the reused descriptors address the same tensors: same results (dK, dV
     # and the forward bit for bit; dq's fp32 reduction order may vary)

@@ -19,7 +19,7 @@ def check(x, res):
     w = x.workload
     O, lse, dq, dk, dv = res
     dq_r, dk_r, dv_r, O_r, lse_r, _ = A.attention_backward(
-        x.q, x.k, x.v, x.do, x.scale, w.causal, x.cu_seqlens, x.alibi_slopes)
+        x.q, x.k, x.v, x.do, x.scale, w.causal, x.cu_seqlens, x.alibi_slopes, window=w.window)
     errs = {}
     if O.size:
         errs["O"] = np.abs(O - O_r).max()
@@ -86,3 +86,54 @@ def test_bwd_repeatable_within_tolerance():
     np.testing.assert_array_equal(r1[3], r2[3])   # dK: fixed order in TMEM
     np.testing.assert_array_equal(r1[4], r2[4])   # dV
     assert np.abs(r1[2] - r2[2]).max() <= 1e-2 * np.abs(r1[2]).max()
+
+
+def _bwd_with_workspace(x, ws_bytes, deterministic):
+    """fa_fwd + fa_bwd with a workspace of exactly ws_bytes; torch tensors."""
+    t = G.torch()
+    from exact_io_aware_36_gb300 import fa
+    w = x.workload
+    q, k, v, do = (G.to_dev(x, n) for n in ("q", "k", "v", "do"))
+    cu = t.from_numpy(x.cu_seqlens).cuda() if w.varlen else None
+    slopes = t.from_numpy(x.alibi_slopes).cuda() if x.alibi_slopes is not None else None
+    kw = dict(causal=w.causal, scale=x.scale, cu_seqlens=cu, max_seqlen=w.N if w.varlen else None,
+              batch=None if w.varlen else w.B, alibi_slopes=slopes, window=w.window, check=True)
+    o, lse = fa.attention_forward(q, k, v, out_dtype=t.float32, **kw)
+    ws = t.empty(ws_bytes, dtype=t.uint8, device="cuda")
+    dq, dk, dv = fa.attention_backward(q, k, v, o, do, lse, workspace=ws,
+                                       deterministic=deterministic, **kw)
+    t.cuda.synchronize()
+    return o, lse, dq, dk, dv
+
+
+@pytest.mark.parametrize("deterministic", [False, True])
+@pytest.mark.parametrize("B,Hq,Hkv,N,d,alibi,seqlens,window", [
+    (2, 8, 1, 700, 128, True, None, None),       # MQA: the group of 8 in two halves
+    (1, 8, 2, 513, 64, False, None, None),
+    (1, 4, 2, 0, 128, False, (300, 1, 129), None),
+    (1, 8, 4, 900, 128, False, None, 200),
+])
+def test_gqa_split_dkdv(B, Hq, Hkv, N, d, alibi, seqlens, window, deterministic):
+    """With fa_bwd_workspace_size_gqa bytes the dK/dV work of each GQA group
+    is split in two blocks whose sums the last stage adds in a fixed order:
+    the oracle's tolerances hold, repeats are bit-identical (dK, dV; dQ too
+    in the deterministic mode), and the result stays within rounding of the
+    unsplit one (the base workspace size)."""
+    from exact_io_aware_36_gb300 import fa
+    w = I.small_case("bf16", causal=True, B=B, Hq=Hq, Hkv=Hkv, N=N, d=d, alibi=alibi,
+                     seqlens=seqlens, window=window)
+    x = I.make_inputs(w, seed=17)
+    base = fa.fa_bwd_workspace_size(w.B, w.Hq, w.N, w.d, x.T)
+    big = fa.fa_bwd_workspace_size_gqa(w.B, w.Hq, w.Hkv, w.N, w.d, x.T)
+    assert big > base
+    r1 = _bwd_with_workspace(x, big, deterministic)
+    r2 = _bwd_with_workspace(x, big, deterministic)
+    r0 = _bwd_with_workspace(x, base, deterministic)
+    t = G.torch()
+    for i in (3, 4) + ((2,) if deterministic else ()):
+        assert t.equal(r1[i], r2[i]), i
+    res = [G.as_f64(a) for a in r1]
+    check(x, res)
+    for i in (2, 3, 4):
+        a, b = res[i], G.as_f64(r0[i])
+        assert np.abs(a - b).max() <= 1e-2 * max(np.abs(b).max(), 1e-30), i

@@ -27,6 +27,21 @@ Inputs (seeded; ``inputs.add_score_structure`` and ``qk_gain``):
 Element-wise against the fp64 oracle at the stated tolerances: O <= 1e-2,
 LSE <= 1e-3 (absolute, O stored as fp32), each gradient <= 2e-2 x that
 gradient's largest |value|.
+
+Limits of the inputs, set by bf16 arithmetic rather than by the method:
+* dQ = scale dS K uses dS rounded to bf16 (relative 2^-9).  The rows of dS
+  sum to zero, so a component that all keys share cancels in exact
+  arithmetic but not after rounding: its part of dQ's error is 2^-9 x the
+  shared component's norm.  The drifting structures give the keys such a
+  component, so the backward uses drifts of 48 nats (rising: 6 nats per
+  128-key tile, still past the forward's threshold of 8 log2 units) and 32
+  nats (falling, with ALiBi), where this effect alone stays below 1 % of
+  max |dQ| (computed from the oracle's dS rounded to bf16); at 200 nats it
+  alone is 2-5 %.
+  The forward keeps the 200-nat drift.
+* LSE is stored as fp32: at |LSE| ~ 10^4 its own rounding is 10^-3.  The
+  non-causal ALiBi case, whose bias is positive for later keys, therefore
+  uses slopes x 8, not x 64 (LSE stays below 2^10).
 """
 import numpy as np
 import pytest
@@ -40,15 +55,17 @@ pytestmark = pytest.mark.gpu
 TOL_O, TOL_LSE, TOL_GRAD = 1e-2, 1e-3, 2e-2
 
 STRENGTH = {"late_dominant": 30.0, "rising": 200.0, "falling": 200.0}
+# backward: drifts whose shared key component bf16 dS can carry (see above)
+BWD_STRENGTH = {"late_dominant": 30.0, "rising": 48.0, "falling": 32.0}
 
 
 def make(kind, *, causal, d, alibi=False, B=1, Hq=4, Hkv=2, N=1024, seqlens=None, gain=1.0,
-         slope_mult=1.0, window=None, seed=0):
+         slope_mult=1.0, window=None, seed=0, strengths=STRENGTH):
     w = I.small_case("bf16", causal=causal, B=B, Hq=Hq, Hkv=Hkv, N=N, d=d, alibi=alibi,
                      seqlens=seqlens, qk_gain=gain, window=window)
     x = I.make_inputs(w, seed=seed)
     if kind is not None:
-        I.add_score_structure(x, kind, STRENGTH[kind], seed=seed + 100)
+        I.add_score_structure(x, kind, strengths[kind], seed=seed + 100)
     if alibi and slope_mult != 1.0:
         x.alibi_slopes = (x.alibi_slopes * np.float32(slope_mult)).astype(np.float32)
     return x
@@ -91,7 +108,7 @@ FWD_CASES = [
     (None, False, 64, False, 8.0, 1.0),
     (None, True, 128, True, 8.0, 1.0),
     (None, True, 128, True, 1.0, 64.0),
-    (None, False, 64, True, 1.0, 64.0),
+    (None, False, 64, True, 1.0, 8.0),
 ]
 
 
@@ -120,7 +137,8 @@ BWD_CASES = [
 @pytest.mark.parametrize("deterministic", [False, True])
 @pytest.mark.parametrize("kind,causal,d,alibi,gain,slope_mult", BWD_CASES)
 def test_backward_peaked(kind, causal, d, alibi, gain, slope_mult, deterministic):
-    x = make(kind, causal=causal, d=d, alibi=alibi, gain=gain, slope_mult=slope_mult, N=1024)
+    x = make(kind, causal=causal, d=d, alibi=alibi, gain=gain, slope_mult=slope_mult, N=1024,
+             strengths=BWD_STRENGTH)
     O, lse, dq, dk, dv = G.backward(x, deterministic=deterministic)
     check_backward(x, O, lse, dq, dk, dv)
 
@@ -128,7 +146,10 @@ def test_backward_peaked(kind, causal, d, alibi, gain, slope_mult, deterministic
 def test_peaked_packed_and_window():
     """The same regimes on a packed batch (sequence starts that are not tile
     aligned) and on a causal band, forward and backward."""
-    x = make("late_dominant", causal=True, d=128, seqlens=(800, 37, 1200, 129), seed=5)
+    x = make("late_dominant", causal=True, d=128, seqlens=(800, 37, 1200, 129), seed=5,
+             strengths=BWD_STRENGTH)
     check_backward(x, *G.backward(x))
-    x = make("rising", causal=True, d=64, N=1500, window=300, seed=6)
+    x = make("rising", causal=True, d=64, N=1024, window=300, seed=6, strengths=BWD_STRENGTH)
     check_backward(x, *G.backward(x))
+    x = make("rising", causal=True, d=128, N=1500, window=300, seed=7)
+    check_forward(x, *G.forward(x))

@@ -85,7 +85,7 @@ def test_repeated_dkdv_stage_recomputes_every_item(deterministic):
     t.cuda.synchronize()
     assert fa.fa_check_device_error(None) == 0
     assert t.equal(dk, dk1) and t.equal(dv, dv1)
-    _, _, _, dk_r, dv_r = G.backward(x, deterministic=bool(deterministic))
+    _, _, _, dk_r, dv_r = G.backward(x, deterministic=bool(deterministic), base_workspace=True)
     assert np.array_equal(G.as_f64(dk), dk_r) and np.array_equal(G.as_f64(dv), dv_r)
 
 
@@ -126,7 +126,7 @@ def test_dkdv_stage_with_a_negative_counter_reports_and_recovers():
     stage(2)
     t.cuda.synchronize()
     assert fa.fa_check_device_error(None) == 0
-    _, _, dq_r, dk_r, dv_r = G.backward(x)
+    _, _, dq_r, dk_r, dv_r = G.backward(x, base_workspace=True)
     assert np.array_equal(G.as_f64(dk), dk_r) and np.array_equal(G.as_f64(dv), dv_r)
     err = np.abs(G.as_f64(dq) - dq_r).max() / max(np.abs(dq_r).max(), 1e-3)
     assert err <= 1e-2, err
