@@ -654,9 +654,10 @@ def run_ours(args, world, rank, local):
     det = 1 if args.deterministic else 0
     # grouped-query problems split their dK/dV items when the workspace has
     # room for the per-part sums; stage 2 then also adds the parts up
-    kv_split = w.backward and ws_bytes > fa.fa_bwd_workspace_size(w.B, w.Hq, w.N, w.d, T)
+    kv_split = fa.fa_bwd_dkdv_split(w.B, w.Hq, w.Hkv, w.N, w.d, w.causal, w.window_arg,
+                                    P(cu), ws_bytes) if w.backward else 1
     names = ["fwd", "bwd_preprocess", "bwd_dkdv",
-             ("bwd_dq" if det else "bwd_dq_convert") + ("+dkdv_convert" if kv_split else "")]
+             ("bwd_dq" if det else "bwd_dq_convert") + ("+dkdv_convert" if kv_split > 1 else "")]
 
     def step(evs=None, ptrs=ptrs):
         if evs is not None:
@@ -791,7 +792,7 @@ def run_ours(args, world, rank, local):
         "data": "synthetic (seeded PCG64, seed 0; no dataset)",
         "config": {"workload": w.name, "desc": w.note, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
                    "N": w.N, "d": w.d, "causal": w.causal, "window": w.window,
-                   "deterministic_bwd": bool(det), "dkdv_split": 2 if kv_split else 1,
+                   "deterministic_bwd": bool(det), "dkdv_split": kv_split,
                    "alibi": w.alibi, "varlen": w.varlen,
                    "total_tokens": T, "o_dtype": "fp32", "flops_per_step": fl["total"],
                    "pct_of_peak": None if fp32 else round(100.0 * value / world / peak, 2),
@@ -803,7 +804,7 @@ def run_ours(args, world, rank, local):
         "per_kernel": per_kernel,
         "roofline": roof,
         "secondary_roofs": None if fp32 else secondary_roofs(w, T, fl, kern_ms, dev, hbm, bool(det)),
-        "gpu_launches": args.steps * ((5 if kv_split else 4) if w.backward else 1),
+        "gpu_launches": args.steps * ((5 if kv_split > 1 and det else 4) if w.backward else 1),
         "clocks": clocks,
         "e2e": e2e,
         "cpu_baseline": cpu,

@@ -79,23 +79,28 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
-def build_variant(name: str, defines, source: str = "fa_fwd_bf16.cu") -> str:
-    """libfa with one source compiled under extra preprocessor `defines`
+def build_variant(name: str, defines, sources=("fa_fwd_bf16.cu",)) -> str:
+    """libfa with some sources compiled under extra preprocessor `defines`
     (e.g. ["FA_FWD_CORRECTION_WARPS=1"]): lib/libfa_<name>.so, sharing the
     other objects of the main build.  For tests of build-time options."""
     build()
-    obj = os.path.join(BUILD, f"variant_{name}.o")
+    if isinstance(sources, str):
+        sources = (sources,)
     out = os.path.join(LIBDIR, f"libfa_{name}.so")
-    src = os.path.join(CSRC, source)
     deps = _deps() + [LIB]
     if os.path.exists(out) and all(os.path.getmtime(f) <= os.path.getmtime(out) for f in deps):
         return out
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *[f"-D{d}" for d in defines], "-c", src, "-o", obj]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"nvcc failed on {source} ({defines}):\n{r.stdout}\n{r.stderr}")
-    objs = [os.path.join(BUILD, os.path.basename(f)[:-3] + ".o") for f in _sources()
-            if os.path.basename(f) != source] + [obj]
+    objs = []
+    for src in sources:
+        obj = os.path.join(BUILD, f"variant_{name}_{src[:-3]}.o")
+        cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *[f"-D{d}" for d in defines], "-c",
+               os.path.join(CSRC, src), "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {src} ({defines}):\n{r.stdout}\n{r.stderr}")
+        objs.append(obj)
+    objs += [os.path.join(BUILD, os.path.basename(f)[:-3] + ".o") for f in _sources()
+             if os.path.basename(f) not in sources]
     tmp = out + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-Xcompiler", "-fPIC", "-cudart", "static", *objs, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)

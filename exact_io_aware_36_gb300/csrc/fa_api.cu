@@ -7,7 +7,10 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <functional>
 #include <mutex>
+#include <queue>
+#include <vector>
 
 #include "fa_host_util.h"
 #include "fa_internal.h"
@@ -145,41 +148,85 @@ size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, long long total_tokens
   return round256((size_t)Hq * T * sizeof(float)) + round256((size_t)Hq * T * d * sizeof(float)) + 256;
 }
 
-// dK / dV work items per (key tile, kv head, sequence) for a group of
-// `group` query heads: 2 (halves of the group) when the group splits evenly.
-static int gqa_split(int Hq, int Hkv) {
+// Largest number of parts the dK/dV work of a GQA group may be split into:
+// 2 when the group splits evenly, else 1 (no split).  (Four parts were
+// measured no faster than two on the GQA workload, B=2 Hq=32 Hkv=4 N=8192,
+// while their sum costs twice as much.)
+static int gqa_split_max(int Hq, int Hkv) {
   const int group = Hkv > 0 ? Hq / Hkv : 0;
   return (group >= 2 && group % 2 == 0) ? 2 : 1;
 }
 
-// Whether the dK/dV work items of a dense batch are too few and too large to
-// spread evenly over the SMs: the largest item (key tile 0: every query tile
-// of every head of the group) against a quarter of the steps per SM.  Each
-// SM takes its next item when it finishes one, largest first; with items
-// this large the last ones leave SMs idle for a good part of an item.
-// Packed batches (sizes unknown on the host) are never split.
-static bool dkdv_items_uneven(int B, int group, int Hkv, int N, int causal, int window) {
+// How many parts to split each dense batch's dK/dV work items into (1 or
+// 2).  The kernel's SMs take items largest first as they finish; with few,
+// large items (a long causal sequence and few kv heads) the last ones leave
+// SMs idle.  For each allowed split this simulates that list schedule over
+// the items' step counts (a step is 64 queries of one head against the key
+// tile), estimates the time as its longest SM in steps, plus the stage that
+// adds the parts up (reads 2 x split fp32 tensors [T, Hkv, d]), and keeps
+// the fastest.  Results are cached per shape.  Packed batches, whose
+// lengths the host does not see, are not split.
+static int dkdv_split(int B, int Hq, int Hkv, int N, int d, int causal, int window) {
+  const int smax = gqa_split_max(Hq, Hkv);
+  if (smax == 1) return 1;
   int nsm = 0;
-  if (fa::sm_count(&nsm) != 0 || nsm <= 0) return false;
+  if (fa::sm_count(&nsm) != 0 || nsm <= 0) return 1;
+  struct Entry { int B, Hq, Hkv, N, d, causal, window, nsm, split; };
+  static Entry cache[16];
+  static int ncache = 0;
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < ncache; ++i) {
+      const Entry& e = cache[i];
+      if (e.B == B && e.Hq == Hq && e.Hkv == Hkv && e.N == N && e.d == d && e.causal == causal &&
+          e.window == window && e.nsm == nsm)
+        return e.split;
+    }
+  }
+  const int group = Hq / Hkv;
   const long long nkt = (N + 127) / 128, nqt_all = (N + 63) / 64;
-  long long total = 0, largest = 0;
+  std::vector<long long> per_kt((size_t)nkt);
   for (long long kt = 0; kt < nkt; ++kt) {
     const long long qt0 = causal ? 2 * kt : 0;
     long long qt_end = nqt_all;
     if (causal && window != fa::kNoWindow)
       qt_end = std::min(nqt_all, (kt * 128 + 127 + window) / 64 + 1);
-    const long long steps = (long long)group * std::max(0ll, qt_end - qt0);
-    total += steps;
-    largest = std::max(largest, steps);
+    per_kt[(size_t)kt] = std::max(0ll, qt_end - qt0);
   }
-  total *= (long long)B * Hkv;
-  return largest * 4 > total / nsm;
+  std::sort(per_kt.begin(), per_kt.end(), std::greater<long long>());
+  const double step_s = 1.6e-6 * d / 128.0;         // measured per-step time of one SM
+  const double bytes_per_s = 6.0e12;                // HBM rate of the adding stage
+  int best = 1;
+  double best_t = 0.0;
+  for (int split = 1; split <= smax; split *= 2) {
+    std::priority_queue<long long, std::vector<long long>, std::greater<long long>> load;
+    for (int i = 0; i < nsm; ++i) load.push(0);
+    const long long per_item = (long long)B * Hkv * split;
+    for (long long steps : per_kt)
+      for (long long i = 0; i < per_item; ++i) {
+        const long long x = load.top();
+        load.pop();
+        load.push(x + steps * group / split);
+      }
+    long long makespan = 0;
+    while (!load.empty()) { makespan = load.top(); load.pop(); }
+    double t = makespan * step_s;
+    if (split > 1) t += (double)split * 2 * B * N * Hkv * d * 4 / bytes_per_s;
+    if (split == 1 || t < best_t) {
+      best = split;
+      best_t = t;
+    }
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  cache[ncache < 16 ? ncache++ : (B + N) % 16] = Entry{B, Hq, Hkv, N, d, causal, window, nsm, best};
+  return best;
 }
 
 size_t fa_bwd_workspace_size_gqa(int B, int Hq, int Hkv, int N, int d, long long total_tokens) {
   const size_t base = fa_bwd_workspace_size(B, Hq, N, d, total_tokens);
   if (base == 0 || Hkv <= 0 || Hq % Hkv != 0) return 0;
-  const int split = gqa_split(Hq, Hkv);
+  const int split = gqa_split_max(Hq, Hkv);
   if (split == 1) return base;
   const long long T = total_tokens > 0 ? total_tokens : (long long)B * N;
   return base + round256((size_t)split * 2 * T * Hkv * d * sizeof(float));
@@ -250,10 +297,9 @@ static fa_status bwd_impl(int stage, const void* q, const void* k, const void* v
   // A workspace of fa_bwd_workspace_size_gqa bytes also holds per-part dK /
   // dV sums, which lets the dK/dV kernel split each GQA group's work.
   p.kv_split = 1;
-  if (!cu_seqlens && gqa_split(Hq, Hkv) > 1 &&
-      dkdv_items_uneven(B, Hq / Hkv, Hkv, N, causal, p.window) &&
-      workspace_bytes >= fa_bwd_workspace_size_gqa(B, Hq, Hkv, N, d, cu_seqlens ? T : 0)) {
-    p.kv_split = gqa_split(Hq, Hkv);
+  if (!cu_seqlens && gqa_split_max(Hq, Hkv) > 1 &&
+      workspace_bytes >= fa_bwd_workspace_size_gqa(B, Hq, Hkv, N, d, 0)) {
+    p.kv_split = dkdv_split(B, Hq, Hkv, N, d, causal, p.window);
     p.dkv_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + need);
   }
   p.status = status_ptr();
@@ -473,6 +519,14 @@ fa_status fa_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {
   unsigned int* status = status_ptr();
   if (!status) return FA_ERR_CUDA;
   return fa::launch_selftest_wait(status, limit_ns, stream) == 0 ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_bwd_dkdv_split(int B, int Hq, int Hkv, int N, int d, int causal, int window,
+                      const int32_t* cu_seqlens, size_t workspace_bytes) {
+  if (B <= 0 || N <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return 1;
+  if (cu_seqlens || gqa_split_max(Hq, Hkv) == 1) return 1;
+  if (workspace_bytes < fa_bwd_workspace_size_gqa(B, Hq, Hkv, N, d, 0)) return 1;
+  return dkdv_split(B, Hq, Hkv, N, d, causal ? 1 : 0, band_width(window, N));
 }
 
 void fa_host_cache_stats(unsigned long long* tmaps_encoded, unsigned long long* tmaps_reused,

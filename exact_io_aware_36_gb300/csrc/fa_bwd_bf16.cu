@@ -176,8 +176,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const AttnParams p)
 
 // ----------------------------------------------------------------- dq convert
 template <int D>
-__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const AttnParams p) {
-  const long long e = (long long)blockIdx.x * 256 + threadIdx.x;   // one per 8 outputs
+__device__ __forceinline__ void dq_convert8(const AttnParams& p, long long e) {
   const long long total = p.T * p.Hq * (D / 8);
   if (e >= total) return;
   const int c8 = (int)(e % (D / 8));
@@ -195,12 +194,16 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const AttnParams p)
   reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dq) + (t * p.Hq + h) * D + c8 * 8)[0] = out;
 }
 
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const AttnParams p) {
+  dq_convert8<D>(p, (long long)blockIdx.x * 256 + threadIdx.x);     // one per 8 outputs
+}
+
 // ------------------------------------------------------- dK/dV parts convert
 // Split dK/dV items (kv_split > 1): dK = scale * sum of the parts, dV = sum of
 // the parts, in part order (deterministic), -> bf16 [T, Hkv, d].
 template <int D>
-__global__ void __launch_bounds__(256) bwd_dkdv_convert_kernel(const AttnParams p) {
-  const long long e = (long long)blockIdx.x * 256 + threadIdx.x;   // one per 8 outputs
+__device__ __forceinline__ void dkdv_convert8(const AttnParams& p, long long e) {
   const long long per = p.T * p.Hkv * (D / 8);
   if (e >= 2 * per) return;
   const int which = e >= per;                    // 0: dK, 1: dV
@@ -222,6 +225,20 @@ __global__ void __launch_bounds__(256) bwd_dkdv_convert_kernel(const AttnParams 
   out.z = pack_bf16x2(a[4] * f, a[5] * f);
   out.w = pack_bf16x2(a[6] * f, a[7] * f);
   reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(which ? p.dv : p.dk) + off)[0] = out;
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dkdv_convert_kernel(const AttnParams p) {
+  dkdv_convert8<D>(p, (long long)blockIdx.x * 256 + threadIdx.x);   // one per 8 outputs
+}
+
+// dq convert and the dK / dV parts' sum in one launch (split work items):
+// the first blocks take dq, the rest dk and dv.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_convert_all_kernel(const AttnParams p, long long n_dq) {
+  const long long e = (long long)blockIdx.x * 256 + threadIdx.x;
+  if (e < n_dq) dq_convert8<D>(p, e);
+  else dkdv_convert8<D>(p, e - n_dq);
 }
 
 // ---------------------------------------------------------------------- dkdv
@@ -850,15 +867,23 @@ int launch_stages(const AttnParams& p, cudaStream_t stream, int stage) {
     if (r) return r;
   }
   if (stage < 0 || stage == 2) {
-    if (p.kv_split > 1) {
-      const long long n8 = 2 * p.T * p.Hkv * (D / 8);
-      bwd_dkdv_convert_kernel<D><<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(p);
-      const cudaError_t e = cudaGetLastError();
-      if (e != cudaSuccess) return (int)e;
+    const long long nkv8 = p.kv_split > 1 ? 2 * p.T * p.Hkv * (D / 8) : 0;
+    if (p.deterministic) {
+      if (nkv8 > 0) {
+        bwd_dkdv_convert_kernel<D><<<(unsigned)((nkv8 + 255) / 256), 256, 0, stream>>>(p);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return (int)e;
+      }
+      return launch_bwd_dq_bf16(p, stream);
     }
-    if (p.deterministic) return launch_bwd_dq_bf16(p, stream);
-    const long long n8 = rows * (D / 8);
-    bwd_dq_convert_kernel<D><<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(p);
+    if (nkv8 == 0) {
+      const long long n8 = rows * (D / 8);
+      bwd_dq_convert_kernel<D><<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(p);
+      return (int)cudaGetLastError();
+    }
+    // dq's blocks first, in whole blocks, then the dK / dV parts
+    const long long n_dq = (rows * (D / 8) + 255) / 256 * 256;
+    bwd_convert_all_kernel<D><<<(unsigned)((n_dq + nkv8 + 255) / 256), 256, 0, stream>>>(p, n_dq);
     return (int)cudaGetLastError();
   }
   return 0;

@@ -27,7 +27,7 @@ STATUS = {
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_stage", "fa_bwd_workspace_size", "fa_check_device_error",
            "fa_status_string", "fa_version", "fa_bwd_static_scratch", "fa_selftest_wait_timeout",
            "fa_decode", "fa_decode_workspace_size", "fa_fp8_layout_get", "fa_fp8_quantize",
-           "fa_fwd_fp8", "fa_host_cache_stats", "fa_bwd_workspace_size_gqa")
+           "fa_fwd_fp8", "fa_host_cache_stats", "fa_bwd_workspace_size_gqa", "fa_bwd_dkdv_split")
 FA_BWD_PREPROCESS, FA_BWD_DKDV, FA_BWD_DQ_CONVERT = 0, 1, 2
 
 
@@ -175,6 +175,14 @@ def fa_bwd_workspace_size(B, Hq, N, d, total_tokens) -> int:
 
 def fa_bwd_workspace_size_gqa(B, Hq, Hkv, N, d, total_tokens) -> int:
     return load().fa_bwd_workspace_size_gqa(B, Hq, Hkv, N, d, total_tokens)
+
+
+def fa_bwd_dkdv_split(B, Hq, Hkv, N, d, causal, window, cu_seqlens, workspace_bytes) -> int:
+    lib = load()
+    fn = lib.fa_bwd_dkdv_split
+    fn.argtypes = [ctypes.c_int] * 7 + [ctypes.c_void_p, ctypes.c_size_t]
+    fn.restype = ctypes.c_int
+    return fn(B, Hq, Hkv, N, d, int(causal), int(window), cu_seqlens, workspace_bytes)
 
 
 def fa_selftest_wait_timeout(limit_ns: int, stream=None) -> int:

@@ -120,20 +120,31 @@ size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, long long total_tokens
 /*
  * A larger workspace for grouped-query problems (Hq / Hkv even and >= 2):
  * fa_bwd_workspace_size plus room for two per-part sums of dK and dV
- * (float32 [2][2][T, Hkv, d]).  Given at least this many bytes, fa_bwd
- * splits the dK/dV work of each (key tile, kv head, sequence) between two
- * blocks, each taking half of the group's query heads; their sums are added
- * in a fixed order by the last stage, so results stay reproducible.  This
- * evens out the work per SM when the group's work items are few and large
- * (e.g. B=2, Hq=32, Hkv=4, N=8192: 512 items of up to 1024 steps on 152
- * SMs).  fa_bwd splits only dense batches whose largest item exceeds a
- * quarter of the average work per SM; otherwise, or with a smaller
- * workspace, the work is not split.  When it is split, FA_BWD_DKDV leaves
- * the parts in the workspace and FA_BWD_DQ_CONVERT writes dk and dv.
- * Returns fa_bwd_workspace_size's value when the problem is never split
- * (Hq / Hkv odd or 1), 0 for invalid sizes.
+ * (float32 [2][2][T, Hkv, d]).  Given at least this many bytes, fa_bwd may
+ * split the dK/dV work of each (key tile, kv head, sequence) of a dense
+ * batch between two blocks, each taking half of the group's query heads;
+ * the parts are added in a fixed order by the last stage, so results stay
+ * reproducible.
+ * This evens out the work per SM when the items are few and large (e.g.
+ * B=2, Hq=32, Hkv=4, N=8192: 512 items of up to 1024 steps on 152 SMs).
+ * Whether to split is decided per shape on the host from a simulation of
+ * the kernel's largest-first schedule, against the cost of adding the
+ * parts.  When work is split, FA_BWD_DKDV leaves the parts in the workspace
+ * and FA_BWD_DQ_CONVERT writes dk and dv.  With a smaller workspace, or for
+ * packed batches, the work is not split.  Returns fa_bwd_workspace_size's
+ * value when the problem is never split (Hq / Hkv odd or 1), 0 for invalid
+ * sizes.
  */
 size_t fa_bwd_workspace_size_gqa(int B, int Hq, int Hkv, int N, int d, long long total_tokens);
+
+/*
+ * The number of parts (1 or 2) fa_bwd splits each dK/dV work item into
+ * for these sizes, mask, packed layout (cu_seqlens NULL or not; it is not
+ * read) and workspace size on the current device; 1 for arguments fa_bwd
+ * would reject.  Diagnostic: callers need not call it.
+ */
+int fa_bwd_dkdv_split(int B, int Hq, int Hkv, int N, int d, int causal, int window,
+                      const int32_t* cu_seqlens, size_t workspace_bytes);
 
 /*
  * Backward: from q, k, v, the forward's o (element type o_dtype) and lse,

@@ -154,6 +154,7 @@ def test_gqa_workspace_size(lib):
     and equals the base size otherwise."""
     base = fa.fa_bwd_workspace_size(2, 32, 8192, 128, 0)
     assert fa.fa_bwd_workspace_size_gqa(2, 32, 4, 8192, 128, 0) == base + 2 * 2 * 16384 * 4 * 128 * 4
+    assert fa.fa_bwd_workspace_size_gqa(2, 32, 16, 8192, 128, 0) == base + 2 * 2 * 16384 * 16 * 128 * 4
     assert fa.fa_bwd_workspace_size_gqa(2, 32, 32, 8192, 128, 0) == base
     assert fa.fa_bwd_workspace_size_gqa(1, 6, 2, 100, 64, 0) == fa.fa_bwd_workspace_size(1, 6, 100, 64, 0)
     assert fa.fa_bwd_workspace_size_gqa(1, 6, 4, 100, 64, 0) == 0        # Hq % Hkv != 0
