@@ -29,7 +29,11 @@ Q1  M = D H: D = diag(s) with s a random vector of +-1 (an input: the random
 Q2  Blocks are 128 consecutive rows of one head within one sequence (the
     last block of a sequence may be shorter); one scale per block:
     scale = amax / 448 in float32 (448 is e4m3's largest finite value), 1 for
-    an all-zero block; code = e4m3(x / scale), the division in float32.
+    an all-zero block.  The values are scaled by the block's reciprocal,
+    inv = 448 / amax (one float32 division per block, 1 for an all-zero
+    block): code = e4m3(x * inv), the product in float32.  (The pages fix no
+    detail of the scaling; a multiply by one reciprocal per block is the
+    usual way to apply a block scale.)
 Q3  e4m3 is the OCP E4M3 format without infinities (bias 7, 3 mantissa bits,
     largest finite 448, smallest subnormal 2^-9); rounding is to nearest,
     ties to even, and values beyond 448 saturate to 448 (the kernel's
@@ -122,8 +126,11 @@ def quantize_blocks(x, cu_seqlens, N):
             r1 = min(r0 + BLOCK, e)
             blk = x[r0:r1]                                      # [rows, H, d]
             amax = np.abs(blk).max(axis=(0, 2)).astype(np.float32)
-            sc = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
-            codes[r0:r1] = e4m3_round((blk / sc[None, :, None]).astype(np.float32))
+            pos = amax > 0
+            safe = np.where(pos, amax, np.float32(1.0)).astype(np.float32)
+            sc = np.where(pos, safe / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+            inv = np.where(pos, np.float32(E4M3_MAX) / safe, np.float32(1.0)).astype(np.float32)
+            codes[r0:r1] = e4m3_round((blk * inv[None, :, None]).astype(np.float32))
             scales[:, b * nblk + i] = sc
     return codes, scales
 

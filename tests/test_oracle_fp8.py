@@ -80,6 +80,15 @@ def test_transform_leaves_scores_unchanged_up_to_d():
     np.testing.assert_allclose(l1, l2, atol=1e-5)
 
 
+def torch_e4m3(x):
+    """PyTorch's float8_e4m3fn rounding of float32 x (None without torch)."""
+    try:
+        import torch
+    except ImportError:
+        return None
+    return torch.tensor(np.asarray(x, dtype=np.float32)).to(torch.float8_e4m3fn).to(torch.float32).numpy()
+
+
 def test_block_quantization_definition():
     lens = [130, 5, 256]
     cu = np.concatenate([[0], np.cumsum(lens)])
@@ -96,6 +105,10 @@ def test_block_quantization_definition():
                 sc = scales[h, b * nblk + i]
                 amax = np.abs(x[r0:r1, h]).max()
                 assert sc == np.float32(amax) / np.float32(448.0)
+                inv = np.float32(448.0) / np.float32(amax)
+                ref = torch_e4m3(x[r0:r1, h] * inv)          # e4m3(x * (448 / amax)), float32
+                if ref is not None:
+                    np.testing.assert_array_equal(codes[r0:r1, h], ref)
                 assert np.abs(codes[r0:r1, h]).max() == 448.0
                 deq = codes[r0:r1, h].astype(np.float64) * sc
                 # half a unit in the last place: 2^-4 relative, or 2^-10 sc near zero
