@@ -12,13 +12,14 @@
 // Every step that decides a code is taken in float32 in a fixed order, so the
 // codes do not depend on the schedule: the sign flip (exact), the butterfly
 // with strides 1, 2, 4, ..., 64 ((a, b) -> (a + b, a - b)), the maximum, the
-// division amax / 448, the division x / scale (IEEE, round to nearest), and
-// the conversion to e4m3 (round to nearest even, saturated).
+// divisions amax / 448 (the stored scale) and 448 / amax (the block's
+// reciprocal, IEEE, round to nearest), the product x * (448 / amax), and the
+// conversion to e4m3 (round to nearest even, saturated).
 //
-// One block of 128 threads per (head, sequence block); a row of d = 128 is one
-// warp, 4 columns per lane: butterfly strides 1 and 2 inside a lane, 4 .. 64
-// across lanes by shuffles.  Two passes over the rows (the maximum, then the
-// codes) recompute the transform instead of holding the block.
+// Two kernels, each one pass over its input with the block's values held in
+// registers from the load to the codes: Q and K with one thread per row
+// (the butterfly entirely in registers), V with one warp per row, 4 columns
+// per lane, and a shared-memory tile for its transposed codes.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -45,39 +46,6 @@ __device__ __forceinline__ bool block_bounds(const QuantParams& p, int b, long l
   return true;
 }
 
-// Row `row` (token) of head h: this lane's 4 columns, optionally sign-flipped
-// and transformed by the butterfly.
-template <bool TRANSFORM>
-__device__ __forceinline__ void load_row(const __nv_bfloat16* x, int H, long long tok, int h,
-                                         const float (&sg)[4], float (&v)[4]) {
-  const int lane = threadIdx.x & 31;
-  const uint2 raw = *reinterpret_cast<const uint2*>(x + (tok * H + h) * kD + 4 * lane);
-  v[0] = __uint_as_float(raw.x << 16);
-  v[1] = __uint_as_float(raw.x & 0xFFFF0000u);
-  v[2] = __uint_as_float(raw.y << 16);
-  v[3] = __uint_as_float(raw.y & 0xFFFF0000u);
-  if constexpr (TRANSFORM) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) v[e] *= sg[e];
-    // stride 1: (0,1), (2,3);  stride 2: (0,2), (1,3)
-    float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
-    v[0] = a0 + a2;
-    v[1] = a1 + a3;
-    v[2] = a0 - a2;
-    v[3] = a1 - a3;
-    // strides 4 .. 64: column c = 4 lane + e pairs with c ^ stride, in lane ^ (stride / 4)
-#pragma unroll
-    for (int sl = 1; sl < 32; sl <<= 1) {
-      const bool upper = (lane & sl) != 0;          // this lane holds the (a, b) pair's b
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float o = __shfl_xor_sync(0xffffffffu, v[e], sl);
-        v[e] = upper ? o - v[e] : v[e] + o;
-      }
-    }
-  }
-}
-
 // Two e4m3 codes of (lo, hi), lo in the low byte.
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   uint16_t r;
@@ -94,55 +62,106 @@ __device__ __forceinline__ float block_amax(float m, float* red) {
   return fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
 }
 
-// Q or K: codes [T, H, 128] and scales [H, B * nblk].  grid (B * nblk, H).
-template <bool TRANSFORM>
-__global__ void __launch_bounds__(kRows) quant_rows_kernel(const QuantParams p, const __nv_bfloat16* x,
-                                                           int H, uint8_t* codes, float* scales) {
+// The block's scale (amax / 448) and the reciprocal its values are scaled
+// by (448 / amax), both 1 for an all-zero block.
+__device__ __forceinline__ void block_scales(float amax, float* scale, float* inv) {
+  *scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  *inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
+}
+
+// Q and K: one thread per row (token) of one head, the whole row of d = 128
+// in registers: the sign flip, the butterfly with strides 1, 2, ..., 64
+// ((a, b) -> (a + b, a - b), a the lower index), the row's |max|, the
+// block's max (128 rows, one block), then codes = e4m3(x * inv) written as
+// 128 bytes per row.  One pass over the input; grid (B * nblk, Hq + Hkv),
+// y < Hq: Q, else K.
+__global__ void __launch_bounds__(kRows, 2) quant_qk_kernel(const QuantParams p) {
   __shared__ float red[4];
-  const int h = blockIdx.y;
+  __shared__ __align__(16) float sg[kD];
+  const bool isq = (int)blockIdx.y < p.Hq;
+  const int h = isq ? blockIdx.y : blockIdx.y - p.Hq;
+  const int H = isq ? p.Hq : p.Hkv;
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(isq ? p.q : p.k);
   const int bi = blockIdx.x;
   const int b = bi / p.nblk;
   const int i = bi % p.nblk;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   long long seq0;
   int L;
   if (!block_bounds(p, b, &seq0, &L)) {
     if (threadIdx.x == 0) record_status(p.status, FA_ERR_CU_SEQLENS);
     return;
   }
-  float* sc_out = scales + (long long)h * p.B * p.nblk + bi;
+  float* sc_out = (isq ? p.q_scale : p.k_scale) + (long long)h * p.B * p.nblk + bi;
   const int r0 = kRows * i;
-  if (r0 >= L) {
+  const int rows = min(kRows, L - r0);
+  if (rows <= 0) {                                 // uniform over the block
     if (threadIdx.x == 0) *sc_out = 1.f;
     return;
   }
-  const int rows = min(kRows, L - r0);
-  float sg[4];
+  sg[threadIdx.x] = __ldg(p.signs + threadIdx.x);
+  const int r = threadIdx.x;
+  const bool valid = r < rows;
+  const long long row = ((seq0 + r0 + r) * H + h) * kD;
+  float v[kD];
+  if (valid) {
+    uint4 raw[kD / 8];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) sg[e] = TRANSFORM ? __ldg(p.signs + 4 * lane + e) : 1.f;
-  float m = 0.f;
-  for (int r = warp; r < rows; r += 4) {
-    float v[4];
-    load_row<TRANSFORM>(x, H, seq0 + r0 + r, h, sg, v);
-    m = fmaxf(m, fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
+    for (int c = 0; c < kD / 8; ++c) raw[c] = reinterpret_cast<const uint4*>(x + row)[c];
+#pragma unroll
+    for (int c = 0; c < kD / 8; ++c) {
+      const uint32_t w[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v[8 * c + 2 * e] = __uint_as_float(w[e] << 16);
+        v[8 * c + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < kD; ++c) v[c] = 0.f;
   }
+  __syncthreads();                                 // sg
+#pragma unroll
+  for (int c = 0; c < kD; ++c) v[c] *= sg[c];
+#pragma unroll
+  for (int st = 0; st < 7; ++st) {                 // strides 1, 2, 4, ..., 64
+    const int hs = 1 << st;
+#pragma unroll
+    for (int k = 0; k < kD / 2; ++k) {             // pair k: (c, c + hs)
+      const int c = (k / hs) * 2 * hs + k % hs;
+      const float a = v[c], bb = v[c + hs];
+      v[c] = a + bb;
+      v[c + hs] = a - bb;
+    }
+  }
+  float m = 0.f;
+#pragma unroll
+  for (int c = 0; c < kD; c += 2) m = fmax3(m, fabsf(v[c]), fabsf(v[c + 1]));
   const float amax = block_amax(m, red);
-  const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  float scale, inv;
+  block_scales(amax, &scale, &inv);
   if (threadIdx.x == 0) *sc_out = scale;
-  for (int r = warp; r < rows; r += 4) {
-    float v[4];
-    const long long tok = seq0 + r0 + r;
-    load_row<TRANSFORM>(x, H, tok, h, sg, v);
-    const uint32_t c01 = e4m3x2(__fdiv_rn(v[0], scale), __fdiv_rn(v[1], scale));
-    const uint32_t c23 = e4m3x2(__fdiv_rn(v[2], scale), __fdiv_rn(v[3], scale));
-    *reinterpret_cast<uint32_t*>(codes + (tok * H + h) * kD + 4 * lane) = c01 | (c23 << 16);
+  if (!valid) return;
+  uint8_t* codes = (isq ? p.q8 : p.k8) + row;
+#pragma unroll
+  for (int c = 0; c < kD; c += 16) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      w[e] = e4m3x2(v[c + 4 * e] * inv, v[c + 4 * e + 1] * inv) |
+             (e4m3x2(v[c + 4 * e + 2] * inv, v[c + 4 * e + 3] * inv) << 16);
+    reinterpret_cast<uint4*>(codes)[c / 16] = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
 // V: codes transposed into [Hkv, 128, B * nblk * 128], scales, and the largest
-// scale per kv head (v_smax, zeroed before).  grid (B * nblk, Hkv).
+// scale per kv head (v_smax, zeroed before).  grid (B * nblk, Hkv).  A warp
+// takes rows warp, warp + 4, ... (4 columns per lane) and keeps them (as
+// bf16) from the load to the codes; the codes go through a shared-memory
+// tile so that each column of 128 keys is written contiguously.
 __global__ void __launch_bounds__(kRows) quant_v_kernel(const QuantParams p) {
   constexpr int kPitch = kRows + 4;               // bytes per column row in the transpose
+  constexpr int kRowsPerWarp = kRows / 4;
   __shared__ float red[4];
   __shared__ __align__(16) uint8_t tile[kD * kPitch];
   const int g = blockIdx.y;
@@ -159,26 +178,35 @@ __global__ void __launch_bounds__(kRows) quant_v_kernel(const QuantParams p) {
   const int r0 = kRows * i;
   const int rows = max(0, min(kRows, L - r0));
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.v);
-  const float sg[4] = {1.f, 1.f, 1.f, 1.f};
   for (int w = threadIdx.x; w < kD * kPitch / 4; w += kRows) reinterpret_cast<uint32_t*>(tile)[w] = 0u;
+  uint2 raw[kRowsPerWarp];
+#pragma unroll
+  for (int j = 0; j < kRowsPerWarp; ++j) {
+    const int r = warp + 4 * j;
+    raw[j] = r < rows ? *reinterpret_cast<const uint2*>(x + ((seq0 + r0 + r) * p.Hkv + g) * kD + 4 * lane)
+                      : make_uint2(0u, 0u);
+  }
   float m = 0.f;
-  for (int r = warp; r < rows; r += 4) {
-    float v[4];
-    load_row<false>(x, p.Hkv, seq0 + r0 + r, g, sg, v);
-    m = fmaxf(m, fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
+#pragma unroll
+  for (int j = 0; j < kRowsPerWarp; ++j) {
+    const float a0 = __uint_as_float(raw[j].x << 16), a1 = __uint_as_float(raw[j].x & 0xFFFF0000u);
+    const float a2 = __uint_as_float(raw[j].y << 16), a3 = __uint_as_float(raw[j].y & 0xFFFF0000u);
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(a2), fabsf(a3))));
   }
   const float amax = block_amax(m, red);          // also orders the zero fill before the codes
-  const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  float scale, inv;
+  block_scales(amax, &scale, &inv);
   if (threadIdx.x == 0) {
     p.v_scale[(long long)g * p.B * p.nblk + bi] = scale;
     if (rows > 0) atomicMax(reinterpret_cast<unsigned int*>(p.v_smax + g), __float_as_uint(scale));
   }
-  for (int r = warp; r < rows; r += 4) {
-    float v[4];
-    load_row<false>(x, p.Hkv, seq0 + r0 + r, g, sg, v);
-    const uint32_t c01 = e4m3x2(__fdiv_rn(v[0], scale), __fdiv_rn(v[1], scale));
-    const uint32_t c23 = e4m3x2(__fdiv_rn(v[2], scale), __fdiv_rn(v[3], scale));
-    const uint32_t c = c01 | (c23 << 16);
+#pragma unroll
+  for (int j = 0; j < kRowsPerWarp; ++j) {
+    const int r = warp + 4 * j;
+    if (r >= rows) break;
+    const float a0 = __uint_as_float(raw[j].x << 16), a1 = __uint_as_float(raw[j].x & 0xFFFF0000u);
+    const float a2 = __uint_as_float(raw[j].y << 16), a3 = __uint_as_float(raw[j].y & 0xFFFF0000u);
+    const uint32_t c = e4m3x2(a0 * inv, a1 * inv) | (e4m3x2(a2 * inv, a3 * inv) << 16);
 #pragma unroll
     for (int e = 0; e < 4; ++e) tile[(4 * lane + e) * kPitch + r] = (uint8_t)(c >> (8 * e));
   }
@@ -197,10 +225,9 @@ int launch_fp8_quantize(const QuantParams& p, void* stream_) {
   cudaError_t e = cudaMemsetAsync(p.v_smax, 0, sizeof(float) * p.Hkv, stream);
   if (e != cudaSuccess) return (int)e;
   const unsigned nb = (unsigned)(p.B * p.nblk);
-  quant_rows_kernel<true><<<dim3(nb, p.Hq), kRows, 0, stream>>>(
-      p, static_cast<const __nv_bfloat16*>(p.q), p.Hq, p.q8, p.q_scale);
-  quant_rows_kernel<true><<<dim3(nb, p.Hkv), kRows, 0, stream>>>(
-      p, static_cast<const __nv_bfloat16*>(p.k), p.Hkv, p.k8, p.k_scale);
+  quant_qk_kernel<<<dim3(nb, p.Hq + p.Hkv), kRows, 0, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return (int)e;
   quant_v_kernel<<<dim3(nb, p.Hkv), kRows, 0, stream>>>(p);
   return (int)cudaGetLastError();
 }

@@ -297,7 +297,8 @@ fa_status fa_decode(const void* q, const void* k_cache, const void* v_cache,
  *                    butterfly in float32); then Q', K' and V are quantized
  *                    to e4m3 per block of 128 rows of one head of one
  *                    sequence, scale = amax / 448 (1 for an all-zero block),
- *                    code = e4m3(x / scale), round to nearest even, saturated.
+ *                    code = e4m3(x * (448 / amax)) (the reciprocal once per
+ *                    block, in float32), round to nearest even, saturated.
  *   fa_fwd_fp8       attention from those codes: S = scale * s_q * s_k
  *                    * (Q8 K8^T) / d, the online softmax of fa_fwd, P rounded
  *                    to e4m3 for the P V product (tensor cores, kind f8f6f4,
