@@ -771,6 +771,17 @@ int launch_impl(const AttnParams& p, cudaStream_t stream) {
   using C = FwdCfg<D, CORR>;
   auto kern = fwd_bf16_kernel<D, CAUSAL, ALIBI, BAND, CORR>;
   if (const int ea = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES)) return ea;
+  // The warpgroups' raised register limits draw on what the CTA is launched
+  // with (threads x registers per thread); a build that allocated fewer
+  // would leave a raise waiting forever, so it is refused here instead.
+  static int regs_ok = -1;
+  if (regs_ok < 0) {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, reinterpret_cast<const void*>(kern)) != cudaSuccess)
+      return (int)cudaErrorInvalidDeviceFunction;
+    regs_ok = a.numRegs >= (CORR ? 128 : 168);
+  }
+  if (!regs_ok) return (int)cudaErrorInvalidConfiguration;
   CUtensorMap tq, tk, tv;
   int r = make_tmap_bf16_3d(&tq, p.q, D, p.Hq, p.T, 128);
   if (!r) r = make_tmap_bf16_3d(&tk, p.k, D, p.Hkv, p.T, 128);
@@ -808,14 +819,19 @@ int launch_fwd_bf16_persistent(const AttnParams& p, void* stream_) {
 // Which forward runs.  The persistent kernel saves a CTA launch, its set-up
 // and the wait for its first loads per work item, and overlaps an item's
 // epilogue with the next item's loads and products; that pays where items
-// are short.  On long dense causal sequences (items of 33 to 128 kv steps at
-// N = 8192 to 32768) one CTA per query block with a TMA-store epilogue is
-// faster (same-box A/B, TFLOP/s, persistent / per block: N = 16384
-// 1304 / 1325; N = 8192 with GQA and ALiBi 1133 / 1190; N = 4096 1078 /
-// 1039; packed lengths of 128-4096 939 / 871; N = 1024, d = 64 346 / 309).
+// are short.  Where items average more than 24 kv steps (long dense causal
+// sequences, N > 6144; wide bands) one CTA per query block with a TMA-store
+// epilogue is faster (same-box A/B, TFLOP/s, persistent / per block:
+// N = 16384 1304 / 1325; N = 8192 with GQA and ALiBi 1133 / 1190; band of
+// 4096 keys at N = 32768 1118 / 1134; N = 4096 1078 / 1039; packed lengths
+// of 128-4096 939 / 871; N = 1024, d = 64 346 / 309).
 int launch_fwd_bf16(const AttnParams& p, void* stream) {
-  const bool long_items = p.cu_seqlens == nullptr && p.N > 4096 &&
-                          (p.window == kNoWindow || p.window >= 4096);
+  // Average kv steps of a dense batch's query blocks of 256 rows: N / 256 + 1
+  // under the causal mask, N / 128 without, at most (w + 256) / 128 + 1 in a
+  // band of width w.  Packed batches always go to the persistent kernel.
+  long long steps = p.causal ? p.N / 256 + 1 : (p.N + 127) / 128;
+  if (p.causal && p.window != kNoWindow) steps = std::min<long long>(steps, (p.window + 256) / 128 + 1);
+  const bool long_items = p.cu_seqlens == nullptr && steps > 24;
   return long_items ? launch_fwd_bf16_block(p, stream) : launch_fwd_bf16_persistent(p, stream);
 }
 
