@@ -102,6 +102,9 @@ WORKLOADS = {
 # Further workloads for the rows beyond the five above: each is checked and
 # measured the same way but is not one of the five.
 EXTRA_WORKLOADS = {
+    "b4_n4096": Workload(
+        "b4_n4096", "bf16", causal=True, B=4, Hq=32, Hkv=32, N=4096, d=128,
+        note="causal, B=4 H=32 N=4096 d=128 (dense batch of the persistent forward's size)"),
     "swa_32k": Workload(
         "swa_32k", "bf16", causal=True, B=1, Hq=32, Hkv=8, N=32768, d=128, window=4095,
         note="sliding window 4096 keys (causal band), GQA 32/8, B=1 N=32768 d=128"),
