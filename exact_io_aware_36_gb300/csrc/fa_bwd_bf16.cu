@@ -72,6 +72,7 @@ struct BwdCfg {
   static constexpr int SIDE_OFF = DQ_OFF + DQ_BYTES;
   static constexpr int BAR_OFF = SIDE_OFF + kQStages * SIDE_BYTES;
   static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per block");
   static constexpr uint32_t DV_COL = 0, DK_COL = D;
   static constexpr uint32_t SB_COL0 = 256, PB_COL0 = 384;   // + 64 * buffer
 };

@@ -51,6 +51,7 @@ struct DqCfg {
   static constexpr int V_OFF = K_OFF + STAGES * KV_TILE;
   static constexpr int BAR_OFF = V_OFF + STAGES * KV_TILE;
   static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per block");
   static constexpr uint32_t S_COL = 0, DP_COL = 128, DQ_COL = 256;   // S, dP: + 64 * buffer
 };
 

@@ -59,6 +59,7 @@ struct Cfg {
   static constexpr int P_OFF = V_OFF + NS * TILE;   // [tile][buffer] P codes
   static constexpr int BAR_OFF = P_OFF + 4 * TILE;
   static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per block");
   // The epilogue stages both tiles' O (fp32 at most) in the K/V slots.
   static_assert(2 * 128 * kD * 4 <= P_OFF - K_OFF, "O staging must fit the K/V slots");
   static constexpr uint32_t S_COL0 = 0, S_COL1 = 128;
