@@ -195,9 +195,9 @@ def ncu_traffic(workload: str, kernel: str):
 
 
 # ncu kernel-name fragment -> (per-kernel key, the source files it is built from).
-# The decode call (split + combine) and the FP8 quantize call (Q, K, then V)
-# launch several kernels; their figures are summed per call, a call being
-# counted by the launches of its last kernel (CALL_LAST).
+# The decode call (split + combine) launches two kernels; their figures are
+# summed per call, a call being counted by the launches of its last kernel
+# (CALL_LAST).
 _COMMON_SOURCES = ["fa_ptx.cuh", "fa_internal.h", "fa_host_util.cu"]
 KERNEL_SOURCES = [
     ("fwd_bf16_block_kernel", "fwd", "fa_fwd_bf16_block.cu"),
@@ -212,7 +212,7 @@ KERNEL_SOURCES = [
     ("quant_", "fp8_quantize", "fa_fp8_quant.cu"),
     ("decode_", "decode", "fa_decode_bf16.cu"),
 ]
-CALL_LAST = {"decode": "combine", "fp8_quantize": "quant_v"}
+CALL_LAST = {"decode": "combine"}
 _BYTE_UNITS = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12}
 _TIME_UNITS = {"ns": 1, "us": 1e3, "usecond": 1e3, "ms": 1e6, "msecond": 1e6, "nsecond": 1}
 
@@ -225,7 +225,7 @@ def record_traffic(csv_path: str, key: str) -> dict:
     """Per-kernel DRAM bytes per launch from an `ncu --csv` metrics log.
 
     Launches of one kernel are averaged; the decode call's split and combine
-    kernels (and the FP8 quantizer's three) are summed per call.  Each
+    kernels are summed per call.  Each
     entry carries a hash of every source the kernel is built from, so that
     ncu_traffic() drops it once the kernel changes."""
     import csv

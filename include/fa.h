@@ -326,7 +326,8 @@ fa_status fa_fp8_layout_get(int B, int Hq, int Hkv, int N, int d, long long tota
 
 /* q, k, v: bf16 as fa_fwd; signs: device float32 [d], each +1 or -1 (the
  * random diagonal D, drawn by the caller); fp8_buf: device, >= total bytes,
- * 256-byte aligned.  Launches three kernels on `stream`. */
+ * 256-byte aligned.  Launches one kernel on `stream` (after a memset of the
+ * per-head maximum V scale). */
 fa_status fa_fp8_quantize(const void* q, const void* k, const void* v, const float* signs,
                           int B, int Hq, int Hkv, int N, int d, const int32_t* cu_seqlens,
                           long long total_tokens, void* fp8_buf, size_t fp8_bytes, void* stream);
