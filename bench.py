@@ -204,9 +204,7 @@ KERNEL_SOURCES = [
     ("fwd_bf16_kernel", "fwd", "fa_fwd_bf16.cu"),
     ("bwd_preprocess_kernel", "bwd_preprocess", "fa_bwd_bf16.cu"),
     ("bwd_dkdv_kernel", "bwd_dkdv", "fa_bwd_bf16.cu"),
-    ("bwd_dq_convert_kernel", "bwd_dq_convert", "fa_bwd_bf16.cu"),
-    ("bwd_convert_all_kernel", "bwd_dq_convert+dkdv_convert", "fa_bwd_bf16.cu"),
-    ("bwd_dkdv_convert_kernel", "bwd_dkdv_convert", "fa_bwd_bf16.cu"),
+    ("bwd_convert_kernel", "bwd_dq_convert", "fa_bwd_bf16.cu"),
     ("bwd_dq_kernel", "bwd_dq", "fa_bwd_dq_bf16.cu"),
     ("fwd_fp8_kernel", "fwd_fp8", "fa_fwd_fp8.cu"),
     ("quant_", "fp8_quantize", "fa_fp8_quant.cu"),

@@ -175,71 +175,85 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const AttnParams p)
   }
 }
 
-// ----------------------------------------------------------------- dq convert
-template <int D>
-__device__ __forceinline__ void dq_convert8(const AttnParams& p, long long e) {
-  const long long total = p.T * p.Hq * (D / 8);
-  if (e >= total) return;
-  const int c8 = (int)(e % (D / 8));
-  const long long th = e / (D / 8);
-  const long long t = th / p.Hq;
-  const int h = (int)(th - t * p.Hq);
-  const float4* src = reinterpret_cast<const float4*>(p.dq_acc + ((long long)h * p.T + t) * D + c8 * 8);
-  const float4 a = src[0], b = src[1];
-  const float s = p.scale;
-  uint4 out;
-  out.x = pack_bf16x2(a.x * s, a.y * s);
-  out.y = pack_bf16x2(a.z * s, a.w * s);
-  out.z = pack_bf16x2(b.x * s, b.y * s);
-  out.w = pack_bf16x2(b.z * s, b.w * s);
-  reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dq) + (t * p.Hq + h) * D + c8 * 8)[0] = out;
-}
+// ------------------------------------------------------------ final outputs
+// One launch: dq = scale * dQacc -> bf16 [T, Hq, d] and, for split dK/dV
+// items (kv_split > 1), dK = scale * the sum of the parts and dV = the sum
+// of the parts, added in part order (deterministic), -> bf16 [T, Hkv, d].
+// A block takes kCvtRows rows of one tensor: the first n_dq blocks dq (rows
+// of one head: contiguous in the accumulator), the rest dK then dV.  D / 8
+// threads share a row, 8 elements each, and every thread issues the loads
+// of its kCvtRows / (256 / (D / 8)) rows before any store.
+constexpr int kCvtRows = 64;
 
 template <int D>
-__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const AttnParams p) {
-  dq_convert8<D>(p, (long long)blockIdx.x * 256 + threadIdx.x);     // one per 8 outputs
-}
-
-// ------------------------------------------------------- dK/dV parts convert
-// Split dK/dV items (kv_split > 1): dK = scale * sum of the parts, dV = sum of
-// the parts, in part order (deterministic), -> bf16 [T, Hkv, d].
-template <int D>
-__device__ __forceinline__ void dkdv_convert8(const AttnParams& p, long long e) {
-  const long long per = p.T * p.Hkv * (D / 8);
-  if (e >= 2 * per) return;
-  const int which = e >= per;                    // 0: dK, 1: dV
-  const long long off = (e - which * per) * 8;   // element offset in [T, Hkv, d]
-  const long long slot = p.T * p.Hkv * D;
-  float a[8];
+__global__ void __launch_bounds__(256) bwd_convert_kernel(const AttnParams p, int nbh, long long n_dq) {
+  constexpr int G = D / 8;                       // threads per row
+  constexpr int RB = 256 / G;                    // rows per pass
+  constexpr int U = kCvtRows / RB;               // rows per thread
+  const int c8 = threadIdx.x % G, rr = threadIdx.x / G;
+  const long long blk = blockIdx.x;
+  if (blk < n_dq) {
+    const int h = (int)(blk / nbh);
+    const long long t0 = (blk % nbh) * kCvtRows;
+    float4 a[U], b[U];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) a[i] = 0.f;
-  for (int r = 0; r < p.kv_split; ++r) {
-    const float4* src = reinterpret_cast<const float4*>(p.dkv_part + (long long)(2 * r + which) * slot + off);
-    const float4 x = src[0], y = src[1];
-    a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
-    a[4] += y.x; a[5] += y.y; a[6] += y.z; a[7] += y.w;
+    for (int u = 0; u < U; ++u) {
+      const long long t = t0 + u * RB + rr;
+      if (t < p.T) {
+        const float4* src = reinterpret_cast<const float4*>(p.dq_acc + ((long long)h * p.T + t) * D + c8 * 8);
+        a[u] = src[0];
+        b[u] = src[1];
+      }
+    }
+    const float s = p.scale;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long t = t0 + u * RB + rr;
+      if (t < p.T)
+        reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dq) + (t * p.Hq + h) * D + c8 * 8)[0] =
+            make_uint4(pack_bf16x2(a[u].x * s, a[u].y * s), pack_bf16x2(a[u].z * s, a[u].w * s),
+                       pack_bf16x2(b[u].x * s, b[u].y * s), pack_bf16x2(b[u].z * s, b[u].w * s));
+    }
+    return;
+  }
+  // dK (which 0) or dV (which 1): rows of [T * Hkv]
+  const long long R = p.T * p.Hkv;
+  const long long nbk = (R + kCvtRows - 1) / kCvtRows;
+  const long long b2 = blk - n_dq;
+  const int which = (int)(b2 / nbk);
+  const long long r0 = (b2 % nbk) * kCvtRows;
+  const long long slot = R * D;
+  constexpr int kMaxParts = 2;
+  float4 x[U][kMaxParts], y[U][kMaxParts];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const long long r = r0 + u * RB + rr;
+#pragma unroll
+    for (int q = 0; q < kMaxParts; ++q)
+      if (r < R && q < p.kv_split) {
+        const float4* src = reinterpret_cast<const float4*>(p.dkv_part + (2 * q + which) * slot + r * D + c8 * 8);
+        x[u][q] = src[0];
+        y[u][q] = src[1];
+      }
   }
   const float f = which ? 1.f : p.scale;
-  uint4 out;
-  out.x = pack_bf16x2(a[0] * f, a[1] * f);
-  out.y = pack_bf16x2(a[2] * f, a[3] * f);
-  out.z = pack_bf16x2(a[4] * f, a[5] * f);
-  out.w = pack_bf16x2(a[6] * f, a[7] * f);
-  reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(which ? p.dv : p.dk) + off)[0] = out;
-}
-
-template <int D>
-__global__ void __launch_bounds__(256) bwd_dkdv_convert_kernel(const AttnParams p) {
-  dkdv_convert8<D>(p, (long long)blockIdx.x * 256 + threadIdx.x);   // one per 8 outputs
-}
-
-// dq convert and the dK / dV parts' sum in one launch (split work items):
-// the first blocks take dq, the rest dk and dv.
-template <int D>
-__global__ void __launch_bounds__(256) bwd_convert_all_kernel(const AttnParams p, long long n_dq) {
-  const long long e = (long long)blockIdx.x * 256 + threadIdx.x;
-  if (e < n_dq) dq_convert8<D>(p, e);
-  else dkdv_convert8<D>(p, e - n_dq);
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const long long r = r0 + u * RB + rr;
+    if (r >= R) continue;
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+#pragma unroll
+    for (int q = 0; q < kMaxParts; ++q)
+      if (q < p.kv_split) {
+        v[0] += x[u][q].x; v[1] += x[u][q].y; v[2] += x[u][q].z; v[3] += x[u][q].w;
+        v[4] += y[u][q].x; v[5] += y[u][q].y; v[6] += y[u][q].z; v[7] += y[u][q].w;
+      }
+    reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(which ? p.dv : p.dk) + r * D + c8 * 8)[0] =
+        make_uint4(pack_bf16x2(v[0] * f, v[1] * f), pack_bf16x2(v[2] * f, v[3] * f),
+                   pack_bf16x2(v[4] * f, v[5] * f), pack_bf16x2(v[6] * f, v[7] * f));
+  }
 }
 
 // ---------------------------------------------------------------------- dkdv
@@ -868,24 +882,18 @@ int launch_stages(const AttnParams& p, cudaStream_t stream, int stage) {
     if (r) return r;
   }
   if (stage < 0 || stage == 2) {
-    const long long nkv8 = p.kv_split > 1 ? 2 * p.T * p.Hkv * (D / 8) : 0;
-    if (p.deterministic) {
-      if (nkv8 > 0) {
-        bwd_dkdv_convert_kernel<D><<<(unsigned)((nkv8 + 255) / 256), 256, 0, stream>>>(p);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return (int)e;
-      }
-      return launch_bwd_dq_bf16(p, stream);
+    // dq (unless deterministic: its own kernel computes it) and the split
+    // parts' sum, in one launch
+    if (p.kv_split > 2) return (int)cudaErrorInvalidValue;     // the sum reads two parts at most
+    const int nbh = (int)((p.T + kCvtRows - 1) / kCvtRows);
+    const long long n_dq = p.deterministic ? 0 : (long long)nbh * p.Hq;
+    const long long n_kv = p.kv_split > 1 ? 2 * ((p.T * p.Hkv + kCvtRows - 1) / kCvtRows) : 0;
+    if (n_dq + n_kv > 0) {
+      bwd_convert_kernel<D><<<(unsigned)(n_dq + n_kv), 256, 0, stream>>>(p, nbh, n_dq);
+      const cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return (int)e;
     }
-    if (nkv8 == 0) {
-      const long long n8 = rows * (D / 8);
-      bwd_dq_convert_kernel<D><<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(p);
-      return (int)cudaGetLastError();
-    }
-    // dq's blocks first, in whole blocks, then the dK / dV parts
-    const long long n_dq = (rows * (D / 8) + 255) / 256 * 256;
-    bwd_convert_all_kernel<D><<<(unsigned)((n_dq + nkv8 + 255) / 256), 256, 0, stream>>>(p, n_dq);
-    return (int)cudaGetLastError();
+    if (p.deterministic) return launch_bwd_dq_bf16(p, stream);
   }
   return 0;
 }
