@@ -8,7 +8,7 @@
 // the output accumulator rescaled when m grows; FA2's L = m + log l saved per
 // row), Key design 4 (FA3-style asynchrony: producer and consumer roles).
 //
-// GB300 mapping (one CTA per SM, 320 threads, 2 query tiles of 128 rows):
+// GB300 mapping (one CTA per SM, 384 threads, 2 query tiles of 128 rows):
 //   warp 9     TMA producer: Q0/Q1 once, then per step j one slot holding
 //              K_j and V_{j-1} (128-byte swizzle), with one full and one
 //              empty mbarrier per slot.  Step j's products are S_t(j), which
@@ -42,9 +42,15 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;     // warps 10, 11 have no role: they complete warpgroup 2
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
+// Register limits per thread after the role split (setmaxnreg): the two
+// softmax warpgroups take what warpgroup 2 (producer, MMA issuer, two idle
+// warps) gives back from the 168 registers every thread is launched with.
+constexpr uint32_t kRegsCtl = 56;
+constexpr uint32_t kRegsSoftmax = 224;
+static_assert(2 * kRegsSoftmax + kRegsCtl <= 3 * 168, "register split (384 threads)");
 constexpr float kTau = 8.0f;
 constexpr float kSpecSum = 256.0f;   // 2^kTau
 
@@ -204,12 +210,15 @@ fwd_bf16_block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
   const uint32_t tmem = bars->tmem_base;
   const WaitCtx wc{&bars->abort_flag, p.status};
 
+  // Every wait below is inlined: code under a raised register limit can hold
+  // no calls.
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ producer
+    regs_lower<kRegsCtl>();
     int issued = early;               // slots whose loads were issued
     for (int j = early; j <= nkv_max; ++j) {
       const int sl = j % C::NS;
-      if (!wait_warp(&bars->kv_empty[sl], ((j / C::NS) & 1) ^ 1, wc)) break;
+      if (!wait_warp_inl(&bars->kv_empty[sl], ((j / C::NS) & 1) ^ 1, wc)) break;
       if (lane == 0) issue_slot(j);
       __syncwarp();
       issued = j + 1;
@@ -220,6 +229,7 @@ fwd_bf16_block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
       wait_warp_drain(&bars->kv_full[j % C::NS], (j / C::NS) & 1);
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
+    regs_lower<kRegsCtl>();
     constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);
     constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, 0, 1);
     const uint32_t sQ = smem_u32(smem + C::Q_OFF);
@@ -231,18 +241,18 @@ fwd_bf16_block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
     const uint64_t qdesc[2] = {smem_desc_sw128(sQ, 16, 1024), smem_desc_sw128(sQ + C::TILE_BYTES, 16, 1024)};
     const uint64_t kdesc0 = smem_desc_sw128(sK, 16, 1024);
     const uint64_t vdesc0 = smem_desc_sw128(sV, C::BOX_BYTES, 1024);
-    bool ok = wait_warp(&bars->q_full, 0, wc);
+    bool ok = wait_warp_inl(&bars->q_full, 0, wc);
     for (int j = 0; ok && j <= nkv_max; ++j) {
       const int sl = j % C::NS;                       // K_j and V_{j-1}
       const uint64_t kdesc = desc_add(kdesc0, sl * C::TILE_BYTES);
       const uint64_t vdesc = desc_add(vdesc0, sl * C::TILE_BYTES);
       // TMA data needs no tcgen05 fence: the MMAs read it once the
       // transaction count of the slot's barrier has completed.
-      if (!(ok = wait_warp(&bars->kv_full[sl], (j / C::NS) & 1, wc))) break;
+      if (!(ok = wait_warp_inl(&bars->kv_full[sl], (j / C::NS) & 1, wc))) break;
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (j >= 1 && j - 1 >= k0[t] && j - 1 < k0[t] + nkv[t]) {
-          if (!(ok = wait_warp(&bars->p_full[t], (j - 1 - k0[t]) & 1, wc))) break;
+          if (!(ok = wait_warp_inl(&bars->p_full[t], (j - 1 - k0[t]) & 1, wc))) break;
           tc_fence_after();
           if (lane == 0) {
 #pragma unroll
@@ -272,8 +282,9 @@ fwd_bf16_block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
     __syncwarp();
     // Tensor-core work must be finished before the TMEM is released.
     wait_warp_drain(&bars->o_done, 0);
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------- softmax
+    regs_raise<kRegsSoftmax>();
     const int t = warp >> 2;
     const int q4 = warp & 3;
     const int row = m0 + 128 * t + 32 * q4 + lane;       // row within the sequence
@@ -288,7 +299,7 @@ fwd_bf16_block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
     float lr = 0.f;    // sum of the bf16-rounded p the PV MMA sees: normalises O
     bool ok = true;
     for (int j = 0; j < nkv[t]; ++j) {        // j: this tile's local step
-      if (!(ok = wait_warp(&bars->s_full[t], j & 1, wc))) break;
+      if (!(ok = wait_warp_inl(&bars->s_full[t], j & 1, wc))) break;
       tc_fence_after();
       uint32_t s[128];
       tmem_ld32(tS + 0, s);
@@ -431,7 +442,7 @@ fwd_bf16_block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
     // that crosses the sequence end keeps per-thread stores of its valid
     // rows (a box would overwrite the next sequence's rows).
     if (nkv[t] > 0) {                          // uniform over the tile's warps
-      if (ok) ok = wait_warp(&bars->o_done, 0, wc);
+      if (ok) ok = wait_warp_inl(&bars->o_done, 0, wc);
       const bool full_tile = m0 + 128 * t + 128 <= L;
       const int r = 32 * q4 + lane;            // row within the tile
       const int esz = p.o_f32 ? 4 : 2;
@@ -499,7 +510,12 @@ fwd_bf16_block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
         }
       }
     }
+  } else {
+    regs_lower<kRegsCtl>();             // warps 10, 11: no role
   }
+  // Every warpgroup returns to the launch limit before the common tail.
+  if (warp < 8) regs_lower<168>();
+  else regs_raise<168>();
 
   tc_fence_before();
   __syncthreads();
@@ -514,6 +530,17 @@ int launch_impl(const AttnParams& p, cudaStream_t stream) {
   using C = FwdCfg<D>;
   auto kern = fwd_bf16_block_kernel<D, CAUSAL, ALIBI, BAND>;
   if (const int ea = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES)) return ea;
+  // The softmax warpgroups' raised register limit draws on what the CTA is
+  // launched with (threads x registers per thread); a build that allocated
+  // fewer would leave the raise waiting forever, so it is refused here.
+  static int regs_ok = -1;
+  if (regs_ok < 0) {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, reinterpret_cast<const void*>(kern)) != cudaSuccess)
+      return (int)cudaErrorInvalidDeviceFunction;
+    regs_ok = a.numRegs >= 168;
+  }
+  if (!regs_ok) return (int)cudaErrorInvalidConfiguration;
   CUtensorMap tq, tk, tv, to;
   int r = make_tmap_bf16_3d(&tq, p.q, D, p.Hq, p.T, 128);
   if (!r) r = make_tmap_bf16_3d(&tk, p.k, D, p.Hkv, p.T, 128);
