@@ -819,19 +819,19 @@ int launch_fwd_bf16_persistent(const AttnParams& p, void* stream_) {
 // Which forward runs.  The persistent kernel saves a CTA launch, its set-up
 // and the wait for its first loads per work item, and overlaps an item's
 // epilogue with the next item's loads and products; that pays where items
-// are short.  Where items average more than 24 kv steps (long dense causal
-// sequences, N > 6144; wide bands) one CTA per query block with a TMA-store
-// epilogue is faster (same-box A/B, TFLOP/s, persistent / per block:
-// N = 16384 1304 / 1325; N = 8192 with GQA and ALiBi 1133 / 1190; band of
-// 4096 keys at N = 32768 1118 / 1134; N = 4096 1078 / 1039; packed lengths
-// of 128-4096 939 / 871; N = 1024, d = 64 346 / 309).
+// are short.  Where items average more than 16 kv steps (dense causal
+// sequences of N > 3840; wide bands) one CTA per query block with a
+// TMA-store epilogue is faster (same-box A/B, TFLOP/s, persistent / per
+// block: N = 16384 1304 / 1414; N = 8192 with GQA and ALiBi 1133 / 1254;
+// N = 4096 1084 - 1091 / 1098; N = 2048 879 / 841; packed lengths of
+// 128-4096 951 / 922; N = 1024, d = 64 346 / 332).
 int launch_fwd_bf16(const AttnParams& p, void* stream) {
   // Average kv steps of a dense batch's query blocks of 256 rows: N / 256 + 1
   // under the causal mask, N / 128 without, at most (w + 256) / 128 + 1 in a
   // band of width w.  Packed batches always go to the persistent kernel.
   long long steps = p.causal ? p.N / 256 + 1 : (p.N + 127) / 128;
   if (p.causal && p.window != kNoWindow) steps = std::min<long long>(steps, (p.window + 256) / 128 + 1);
-  const bool long_items = p.cu_seqlens == nullptr && steps > 24;
+  const bool long_items = p.cu_seqlens == nullptr && steps > 16;
   return long_items ? launch_fwd_bf16_block(p, stream) : launch_fwd_bf16_persistent(p, stream);
 }
 
