@@ -120,6 +120,31 @@ def test_forward_peaked(kind, causal, d, alibi, gain, slope_mult):
     check_forward(x, O, lse)
 
 
+# The same regimes on shapes the per-block forward takes (more than 16 kv
+# steps per 256-row query block on average: causal N >= 4096, non-causal
+# N > 2048); the drift is doubled so that the max still rises by more than
+# tau per 128-key tile over the longer sequence.
+BLOCK_STRENGTH = {"late_dominant": 30.0, "rising": 400.0, "falling": 400.0}
+FWD_BLOCK_CASES = [
+    # kind, causal, d, alibi, gain, slope_mult, N
+    ("late_dominant", True, 128, False, 1.0, 1.0, 4100),
+    ("rising", True, 64, False, 1.0, 1.0, 4100),
+    ("rising", False, 128, False, 1.0, 1.0, 2200),
+    ("falling", True, 128, True, 1.0, 1.0, 4100),
+    (None, False, 64, False, 8.0, 1.0, 2200),
+    (None, True, 128, True, 1.0, 64.0, 4100),
+]
+
+
+@pytest.mark.parametrize("kind,causal,d,alibi,gain,slope_mult,N", FWD_BLOCK_CASES)
+def test_forward_peaked_block_kernel(kind, causal, d, alibi, gain, slope_mult, N):
+    assert (N // 256 + 1 if causal else (N + 127) // 128) > 16     # the per-block kernel
+    x = make(kind, causal=causal, d=d, alibi=alibi, gain=gain, slope_mult=slope_mult, N=N,
+             Hq=2, Hkv=1, strengths=BLOCK_STRENGTH, seed=11)
+    O, lse = G.forward(x)
+    check_forward(x, O, lse)
+
+
 BWD_CASES = [
     # kind, causal, d, alibi, gain, slope_mult
     ("late_dominant", True, 128, False, 1.0, 1.0),
